@@ -1,0 +1,176 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 speculative-decoding verification
+ * library (libspecverify.so).
+ *
+ * The operation is the verification step of speculative decoding as the
+ * tutorial page at http://www.dpshk.com/news/5598276/ ("P3"; its HTML title,
+ * 企业官网建设流程全解析, is unrelated to its content) defines it:
+ *   P3 §3.1 steps 2-4 and §5.2 steps (1)-(5):
+ *     p_i   = softmax(target_logits[b, i, :] / T_b)              (i <= g_b)
+ *     a_i   = min(1, p_i(x_i) / max(q_i(x_i), 1e-10))            (i <  g_b)
+ *     keep  x_i while u_i < a_i; k_b = first i with u_i >= a_i (else g_b)
+ *     token at k_b: drawn from (p_k - q_k)_+ / sum (p_k - q_k)_+ on a
+ *     rejection, from p_{g_b} (the bonus row, §5.3) when all are kept.
+ *   Draws are inverse-CDF draws on the caller's uniform u_s[b]: the token is
+ *   the smallest j whose inclusive prefix sum of the (unnormalised) weights
+ *   exceeds u_s[b] times their total.  T_b = 0 is greedy decoding (P3 §8,
+ *   pitfall 2): p is one-hot at the lowest-index maximum logit.
+ *
+ * Conventions for every entry point:
+ *   - All tensor arguments are DEVICE pointers to dense row-major arrays,
+ *     owned by the caller; the library allocates nothing and keeps no state
+ *     between calls.  The caller also owns the workspace and the stream.
+ *   - Work is enqueued asynchronously on `stream` (NULL = legacy default
+ *     stream).  Host-side argument checks return an error before anything is
+ *     enqueued; a failed launch returns SV_ERR_CUDA.
+ *   - Invalid per-request DATA (a draft length outside [0, gamma_max], a
+ *     temperature that is negative, NaN, inf or subnormal, a draft token id
+ *     outside [0, V), a uniform outside [0, 1), a non-finite softmax
+ *     normaliser) never traps: that request gets out_num_accepted = -1 and an
+ *     all -1 token row, other requests are unaffected, and the matching
+ *     SV_BAD_* bit is set in the workspace's error word (sv_last_error).
+ *   - Outputs must not alias inputs or the workspace.  Calls that share one
+ *     workspace must be ordered on one stream.
+ *   - Logits must be finite for greedy rows (T = 0); for T > 0 a NaN or +inf
+ *     logit marks the request bad, and -inf logits are allowed (masked
+ *     tokens) as long as each row has a finite maximum.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SV_API __attribute__((visibility("default")))
+#else
+#define SV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (a CUstream handle); NULL = default stream. */
+typedef struct CUstream_st *sv_stream_t;
+
+typedef enum {
+    SV_OK = 0,
+    SV_ERR_INVALID_ARG = 1,        /* NULL pointer, negative size, misaligned
+                                      workspace, sizes beyond int32 indexing */
+    SV_ERR_UNSUPPORTED_DTYPE = 2,  /* logits_dtype is not SV_F32 / SV_BF16 */
+    SV_ERR_WORKSPACE_TOO_SMALL = 3,/* workspace_bytes < sv_workspace_bytes() */
+    SV_ERR_CUDA = 4,               /* a CUDA runtime call or launch failed */
+    SV_ERR_TIMEOUT = 5,            /* a bounded device-side wait ran out */
+    SV_ERR_BAD_INPUT_DATA = 6      /* some request had invalid data */
+} sv_status;
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+/* Bits of the device error word read back by sv_last_error(). */
+#define SV_BAD_DRAFT_LEN 0x1u    /* draft_lens[b] outside [0, gamma_max]     */
+#define SV_BAD_TEMPERATURE 0x2u  /* T negative, NaN, inf or subnormal       */
+#define SV_BAD_TOKEN 0x4u        /* a draft token id outside [0, V)         */
+#define SV_BAD_U_ACCEPT 0x8u     /* an acceptance uniform outside [0, 1)    */
+#define SV_BAD_U_SAMPLE 0x10u    /* the sampling uniform outside [0, 1)     */
+#define SV_BAD_NORMALISER 0x20u  /* non-finite softmax normaliser (T > 0)   */
+#define SV_FAULT_TIMEOUT 0x10000u/* a bounded wait inside a kernel gave up  */
+
+/*
+ * Workspace size in bytes for a batch of B requests with up to gamma_max
+ * drafts each over a V-token vocabulary (any logits dtype).  The workspace
+ * must be device memory aligned to 256 bytes.  It needs no initialisation:
+ * every call resets the parts it reads.  Returns 0 for invalid sizes.
+ */
+SV_API size_t sv_workspace_bytes(int B, int gamma_max, int V);
+
+/*
+ * One verification step for a batch (P3 §3.1, §5.2, §5.3).
+ *
+ *   target_logits    [B, gamma_max+1, V]  logits_dtype (fp32 or bf16).  Row
+ *                    i of request b is the target model's output after the
+ *                    prefix and drafts x_0..x_{i-1}; row g_b is the bonus row.
+ *                    Rows past g_b are never read.
+ *   draft_token_ids  [B, gamma_max] int32: x_i, the drafted tokens.
+ *   draft_probs      [B, gamma_max, V] fp32: q_i, the draft model's
+ *                    distribution at each drafted position, already at the
+ *                    draft's own temperature.  NULL means deterministic
+ *                    drafts (prompt lookup, P3 §7): q_i is one-hot at x_i.
+ *   uniforms_accept  [B, gamma_max] fp32 in [0, 1): the accept test's dice.
+ *   uniforms_sample  [B] fp32 in [0, 1): the resample or bonus draw.
+ *   temperature      [B] fp32: T_b >= 0, divides the target logits; 0 is
+ *                    greedy.
+ *   draft_lens       [B] int32 g_b in [0, gamma_max], or NULL: every request
+ *                    drafts gamma_max tokens.  g_b = 0 is plain sampling from
+ *                    row 0.
+ *   B, gamma_max, V  B >= 0 (0 is a no-op), gamma_max >= 0, V >= 1, with
+ *                    B*(gamma_max+1) and V below 2^31.
+ *   out_tokens       [B, gamma_max+1] int32: x_0..x_{k-1}, then the
+ *                    resampled, bonus or argmax token at position k, then -1.
+ *   out_num_accepted [B] int32: k_b, or -1 for a request with invalid data.
+ *   workspace        device scratch of at least sv_workspace_bytes(B,
+ *                    gamma_max, V) bytes, 256-byte aligned.
+ *
+ * Arithmetic is fp32 (bf16 logits widen exactly); accept decisions and drawn
+ * tokens equal an exact-arithmetic evaluation except where the decision
+ * margin (|u - a|, or the distance of u*S to a CDF edge) is of the order of
+ * fp32 rounding.  Results are deterministic for identical inputs.
+ */
+SV_API sv_status spec_verify(const void *target_logits, sv_dtype logits_dtype,
+                      const int32_t *draft_token_ids, const float *draft_probs,
+                      const float *uniforms_accept,
+                      const float *uniforms_sample, const float *temperature,
+                      const int32_t *draft_lens, int B, int gamma_max, int V,
+                      int32_t *out_tokens, int32_t *out_num_accepted,
+                      void *workspace, size_t workspace_bytes,
+                      sv_stream_t stream);
+
+/*
+ * Optional diagnostic outputs (device pointers; any may be NULL).  Slots a
+ * request does not use hold NaN (floats), 2 (flags) or -1 (indices).
+ */
+typedef struct {
+    float *p_tok;        /* [B, gamma_max]   p_i(x_i)                        */
+    float *q_tok;        /* [B, gamma_max]   q_i(x_i) before the 1e-10 clamp */
+    float *accept_prob;  /* [B, gamma_max]   a_i                             */
+    uint8_t *flags;      /* [B, gamma_max]   1 accepted, 0 rejected (every
+                                             position < g_b is evaluated)    */
+    float *row_max;      /* [B, gamma_max+1] max_j logit                     */
+    float *row_sum;      /* [B, gamma_max+1] sum_j exp((l_j - max) / T); 1
+                                             for greedy rows                 */
+    int32_t *row_argmax; /* [B, gamma_max+1] lowest argmax (greedy rows
+                                             only; -1 for T > 0 rows)        */
+    float *resid_mass;   /* [B] S = sum_j (p_k - q_k)_+ of the draw (NaN for
+                                greedy requests)                             */
+} sv_diag;
+
+/* spec_verify plus the diagnostic outputs in `diag` (may be NULL). */
+SV_API sv_status spec_verify_diag(const void *target_logits, sv_dtype logits_dtype,
+                           const int32_t *draft_token_ids,
+                           const float *draft_probs,
+                           const float *uniforms_accept,
+                           const float *uniforms_sample,
+                           const float *temperature, const int32_t *draft_lens,
+                           int B, int gamma_max, int V, int32_t *out_tokens,
+                           int32_t *out_num_accepted, void *workspace,
+                           size_t workspace_bytes, sv_stream_t stream,
+                           const sv_diag *diag);
+
+/*
+ * Reads the error word of the last call that used `workspace` (synchronises
+ * `stream`).  *out_word (may be NULL) receives the SV_BAD_* / SV_FAULT_*
+ * bits.  Returns SV_ERR_TIMEOUT if a bounded wait gave up, else
+ * SV_ERR_BAD_INPUT_DATA if any request had invalid data, else SV_OK
+ * (SV_ERR_CUDA if the copy fails, SV_ERR_INVALID_ARG for a NULL workspace).
+ */
+SV_API sv_status sv_last_error(const void *workspace, sv_stream_t stream,
+                        uint32_t *out_word);
+
+/* Static, human-readable name of a status code. */
+SV_API const char *sv_status_string(sv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

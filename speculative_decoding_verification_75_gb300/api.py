@@ -1,0 +1,251 @@
+"""Python binding of libspecverify.so (argument marshalling only).
+
+Every step of the verification runs in the library's CUDA kernels; this
+module checks tensor shapes and dtypes, allocates outputs and a workspace
+with PyTorch, and passes raw device pointers plus the current CUDA stream to
+the C ABI declared in ``include/spec_verify.h``.  There is no fallback: if
+the library is not built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+SV_OK = 0
+SV_ERR_INVALID_ARG = 1
+SV_ERR_UNSUPPORTED_DTYPE = 2
+SV_ERR_WORKSPACE_TOO_SMALL = 3
+SV_ERR_CUDA = 4
+SV_ERR_TIMEOUT = 5
+SV_ERR_BAD_INPUT_DATA = 6
+
+SV_F32 = 0
+SV_BF16 = 1
+
+SV_BAD_DRAFT_LEN = 0x1
+SV_BAD_TEMPERATURE = 0x2
+SV_BAD_TOKEN = 0x4
+SV_BAD_U_ACCEPT = 0x8
+SV_BAD_U_SAMPLE = 0x10
+SV_BAD_NORMALISER = 0x20
+SV_FAULT_TIMEOUT = 0x10000
+
+# Every symbol include/spec_verify.h declares.
+EXPORTS = ("sv_workspace_bytes", "spec_verify", "spec_verify_diag",
+           "sv_last_error", "sv_status_string")
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+
+
+class SvDiag(ctypes.Structure):
+    """Mirror of ``sv_diag``: device pointers, any may be NULL."""
+    _fields_ = [("p_tok", _P), ("q_tok", _P), ("accept_prob", _P),
+                ("flags", _P), ("row_max", _P), ("row_sum", _P),
+                ("row_argmax", _P), ("resid_mass", _P)]
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, status: int, lib):
+        self.status = status
+        super().__init__(lib.sv_status_string(status).decode())
+
+
+_lib = None
+
+
+def library_path() -> Path:
+    return _build.LIB
+
+
+def load_library():
+    """Load libspecverify.so (it must have been built); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not path.exists():
+        raise RuntimeError(
+            f"{path} is not built: run `python -m "
+            "speculative_decoding_verification_75_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(str(path))
+    lib.sv_workspace_bytes.restype = ctypes.c_size_t
+    lib.sv_workspace_bytes.argtypes = [_I, _I, _I]
+    common = [_P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P,
+              ctypes.c_size_t, _P]
+    lib.spec_verify.restype = _I
+    lib.spec_verify.argtypes = common
+    lib.spec_verify_diag.restype = _I
+    lib.spec_verify_diag.argtypes = common + [ctypes.POINTER(SvDiag)]
+    lib.sv_last_error.restype = _I
+    lib.sv_last_error.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.sv_status_string.restype = ctypes.c_char_p
+    lib.sv_status_string.argtypes = [_I]
+    _lib = lib
+    return lib
+
+
+def workspace_bytes(B: int, gamma_max: int, V: int) -> int:
+    return int(load_library().sv_workspace_bytes(B, gamma_max, V))
+
+
+def status_string(status: int) -> str:
+    return load_library().sv_status_string(status).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream], device) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+_ws_cache: dict = {}
+
+
+def get_workspace(B: int, gamma_max: int, V: int, device) -> torch.Tensor:
+    """A cached uint8 device buffer of at least sv_workspace_bytes() bytes."""
+    need = workspace_bytes(B, gamma_max, V)
+    dev = torch.device(device)
+    ws = _ws_cache.get(dev)
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        _ws_cache[dev] = ws
+    return ws
+
+
+def _check(t: Optional[torch.Tensor], name, dtype, shape, device):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def verify(target_logits: torch.Tensor, draft_token_ids: torch.Tensor,
+           draft_probs: Optional[torch.Tensor], uniforms_accept: torch.Tensor,
+           uniforms_sample: torch.Tensor, temperature: torch.Tensor,
+           draft_lens: Optional[torch.Tensor] = None, *,
+           out_tokens: Optional[torch.Tensor] = None,
+           out_num_accepted: Optional[torch.Tensor] = None,
+           workspace: Optional[torch.Tensor] = None, diag: bool = False,
+           stream: Optional[torch.cuda.Stream] = None):
+    """One speculative-decoding verification step on CUDA tensors.
+
+    target_logits [B, g+1, V] bf16/fp32, draft_token_ids [B, g] int32,
+    draft_probs [B, g, V] fp32 or None (deterministic drafts),
+    uniforms_accept [B, g] fp32, uniforms_sample [B] fp32,
+    temperature [B] fp32, draft_lens [B] int32 or None.
+
+    Returns (out_tokens [B, g+1] int32, out_num_accepted [B] int32), plus a
+    dict of diagnostic tensors when ``diag`` is true.  Asynchronous on the
+    current (or given) stream.
+    """
+    lib = load_library()
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be [B, gamma_max+1, V]")
+    B, R, V = target_logits.shape
+    g = R - 1
+    dev = target_logits.device
+    if dev.type != "cuda":
+        raise ValueError("verify() takes CUDA tensors; see verify_host()")
+    if target_logits.dtype == torch.bfloat16:
+        dt = SV_BF16
+    elif target_logits.dtype == torch.float32:
+        dt = SV_F32
+    else:
+        raise TypeError(f"unsupported logits dtype {target_logits.dtype}")
+    _check(target_logits, "target_logits", target_logits.dtype, (B, R, V), dev)
+    _check(draft_token_ids, "draft_token_ids", torch.int32, (B, g), dev)
+    _check(draft_probs, "draft_probs", torch.float32, (B, g, V), dev)
+    _check(uniforms_accept, "uniforms_accept", torch.float32, (B, g), dev)
+    _check(uniforms_sample, "uniforms_sample", torch.float32, (B,), dev)
+    _check(temperature, "temperature", torch.float32, (B,), dev)
+    _check(draft_lens, "draft_lens", torch.int32, (B,), dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(B, R, dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    _check(out_tokens, "out_tokens", torch.int32, (B, R), dev)
+    _check(out_num_accepted, "out_num_accepted", torch.int32, (B,), dev)
+    if workspace is None:
+        workspace = get_workspace(B, g, V, dev)
+    args = [_ptr(target_logits), dt, _ptr(draft_token_ids), _ptr(draft_probs),
+            _ptr(uniforms_accept), _ptr(uniforms_sample), _ptr(temperature),
+            _ptr(draft_lens), B, g, V, _ptr(out_tokens), _ptr(out_num_accepted),
+            _ptr(workspace), workspace.numel(), _stream_handle(stream, dev)]
+    d = None
+    if diag:
+        f32 = dict(dtype=torch.float32, device=dev)
+        d = {"p_tok": torch.empty(B, g, **f32), "q_tok": torch.empty(B, g, **f32),
+             "accept_prob": torch.empty(B, g, **f32),
+             "flags": torch.empty(B, g, dtype=torch.uint8, device=dev),
+             "row_max": torch.empty(B, R, **f32), "row_sum": torch.empty(B, R, **f32),
+             "row_argmax": torch.empty(B, R, dtype=torch.int32, device=dev),
+             "resid_mass": torch.empty(B, **f32)}
+        sd = SvDiag(**{k: v.data_ptr() for k, v in d.items()})
+        rc = lib.spec_verify_diag(*args, ctypes.byref(sd))
+    else:
+        rc = lib.spec_verify(*args)
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, lib)
+    if diag:
+        return out_tokens, out_num_accepted, d
+    return out_tokens, out_num_accepted
+
+
+def verify_host(target_logits: torch.Tensor, draft_token_ids: torch.Tensor,
+                draft_probs: Optional[torch.Tensor], uniforms_accept: torch.Tensor,
+                uniforms_sample: torch.Tensor, temperature: torch.Tensor,
+                draft_lens: Optional[torch.Tensor] = None, *, device="cuda",
+                stream: Optional[torch.cuda.Stream] = None):
+    """``verify`` for host tensors (pinned for asynchronous copies): copies
+    the inputs to ``device``, runs the step there and copies the two outputs
+    back.  Returns host (out_tokens, out_num_accepted) once they are ready."""
+    dev = torch.device(device)
+
+    def up(t):
+        return None if t is None else t.to(dev, non_blocking=True)
+
+    with torch.cuda.stream(stream) if stream is not None else _nullctx():
+        tok, nacc = verify(up(target_logits), up(draft_token_ids), up(draft_probs),
+                           up(uniforms_accept), up(uniforms_sample), up(temperature),
+                           up(draft_lens), stream=stream)
+        tok_h = torch.empty(tok.shape, dtype=tok.dtype, pin_memory=True)
+        nacc_h = torch.empty(nacc.shape, dtype=nacc.dtype, pin_memory=True)
+        tok_h.copy_(tok, non_blocking=True)
+        nacc_h.copy_(nacc, non_blocking=True)
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        s.synchronize()
+    return tok_h, nacc_h
+
+
+class _nullctx:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def last_error(workspace: torch.Tensor, stream: Optional[torch.cuda.Stream] = None):
+    """(status, error word) of the last call that used ``workspace``."""
+    lib = load_library()
+    word = ctypes.c_uint32(0)
+    rc = lib.sv_last_error(_ptr(workspace), _stream_handle(stream, workspace.device),
+                           ctypes.byref(word))
+    return rc, word.value

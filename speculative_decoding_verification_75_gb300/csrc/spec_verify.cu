@@ -1,0 +1,218 @@
+// spec_verify.cu -- C ABI of the GB300 speculative-decoding verification
+// library: argument checks, workspace carving and the three launches.
+//
+//   kernel 0  sv_prepare_kernel    reset per-call counters, reject bad lengths
+//   kernel 1  sv_rowstats_kernel   softmax statistics of every row, accept
+//                                  test and first rejection per request
+//   kernel 2  sv_resample_kernel   residual / bonus draw for sampled requests
+//
+// Kernels 1 and 2 are launched with programmatic stream serialisation so
+// that each one's launch and prologue overlap the tail of its predecessor.
+// Each of them comes in a TMA variant (rows start on 16-byte boundaries) and
+// a plain-load variant for any other alignment.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cstdint>
+
+#include "spec_verify.h"
+#include "sv_device.cuh"
+#include "sv_layout.cuh"
+#include "sv_prepare.cuh"
+#include "sv_resample.cuh"
+#include "sv_rowstats.cuh"
+
+namespace sv {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+bool sizes_ok(int B, int gmax, int V) {
+  if (B < 0 || gmax < 0 || V < 1) return false;
+  const long long rows = static_cast<long long>(B) * (gmax + 1);
+  return rows < INT_MAX && static_cast<long long>(gmax) * V < (1ll << 62);
+}
+
+bool aligned(const void *p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+// Raise the dynamic shared-memory limit of a kernel once per device.
+template <typename K>
+cudaError_t ensure_smem(K kernel, size_t bytes, std::atomic<uint64_t> &done, int dev) {
+  const uint64_t bit = 1ull << (dev % kMaxDevices);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(bytes));
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+template <typename K>
+cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       const Params &p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+template <typename T, bool kTMA>
+sv_status launch_all(Params &p, cudaStream_t st, int dev, int nsm) {
+  static std::atomic<uint64_t> k1_done{0}, k2_done{0};
+  constexpr int kChunk = Elem<T>::kChunk;
+  p.C = div_up(p.V, kChunk);
+  p.C2 = div_up(p.V, kK2Chunk);
+  p.nseg = div_up(p.V, kSeg);
+
+  auto *k1 = sv_rowstats_kernel<T, kTMA>;
+  auto *k2 = sv_resample_kernel<T, kTMA>;
+  const size_t s1 = k1_smem_bytes();
+  const size_t s2 = k2_smem_bytes<T>(kTMA);
+  if (ensure_smem(k1, s1, k1_done, dev) != cudaSuccess ||
+      ensure_smem(k2, s2, k2_done, dev) != cudaSuccess)
+    return SV_ERR_CUDA;
+
+  sv_prepare_kernel<<<1, kPrepThreads, 0, st>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+
+  const long long max_items = static_cast<long long>(p.B) * (p.gmax + 1) * p.C;
+  const int g1 = static_cast<int>(max_items < nsm ? max_items : nsm);
+  if (launch_pdl(k1, dim3(g1), dim3(kK1Threads), s1, st, p) != cudaSuccess)
+    return SV_ERR_CUDA;
+
+  const long long max_items2 = static_cast<long long>(p.B) * p.C2;
+  const int g2 = static_cast<int>(max_items2 < nsm ? max_items2 : nsm);
+  if (launch_pdl(k2, dim3(g2), dim3(K2Shape<T>::kThreads), s2, st, p) != cudaSuccess)
+    return SV_ERR_CUDA;
+  return SV_OK;
+}
+
+sv_status run(const void *logits, sv_dtype dtype, const int32_t *ids, const float *q,
+              const float *u_acc, const float *u_smp, const float *temp,
+              const int32_t *lens, int B, int gmax, int V, int32_t *out_tokens,
+              int32_t *out_nacc, void *ws, size_t ws_bytes, sv_stream_t stream,
+              const sv_diag *diag) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_UNSUPPORTED_DTYPE;
+  if (!sizes_ok(B, gmax, V)) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!logits || !u_smp || !temp || !out_tokens || !out_nacc || !ws)
+    return SV_ERR_INVALID_ARG;
+  if (gmax > 0 && (!ids || !u_acc)) return SV_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return SV_ERR_INVALID_ARG;
+  const size_t esz = dtype == SV_BF16 ? 2 : 4;
+  if (!aligned(logits, esz) || (q && !aligned(q, 4))) return SV_ERR_INVALID_ARG;
+  const Layout L = make_layout(B, gmax, V);
+  if (ws_bytes < L.total) return SV_ERR_WORKSPACE_TOO_SMALL;
+
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SV_ERR_CUDA;
+
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  Params p{};
+  p.logits = logits;
+  p.ids = ids;
+  p.q = q;
+  p.u_acc = u_acc;
+  p.u_smp = u_smp;
+  p.temp = temp;
+  p.lens = lens;
+  p.B = B;
+  p.gmax = gmax;
+  p.V = V;
+  p.out_tokens = out_tokens;
+  p.out_nacc = out_nacc;
+  if (diag) p.diag = *diag;
+  p.hdr = reinterpret_cast<Header *>(w + L.hdr);
+  p.k1_cnt = reinterpret_cast<uint32_t *>(w + L.k1_cnt);
+  p.k2_cnt = reinterpret_cast<uint32_t *>(w + L.k2_cnt);
+  p.desc_q = reinterpret_cast<Desc *>(w + L.desc_q);
+  p.desc_noq = reinterpret_cast<Desc *>(w + L.desc_noq);
+  p.part1 = reinterpret_cast<Part *>(w + L.part1);
+  p.csum = reinterpret_cast<float2 *>(w + L.csum);
+  p.ssum = reinterpret_cast<float2 *>(w + L.ssum);
+
+  // TMA bulk copies need 16-byte aligned rows: the base pointers and the
+  // row pitch of the logits (and of q, when present).
+  const bool tma = aligned(logits, 16) && (static_cast<size_t>(V) * esz) % 16 == 0 &&
+                   (!q || (aligned(q, 16) && (static_cast<size_t>(V) * 4) % 16 == 0));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == SV_BF16)
+    return tma ? launch_all<__nv_bfloat16, true>(p, st, dev, nsm)
+               : launch_all<__nv_bfloat16, false>(p, st, dev, nsm);
+  return tma ? launch_all<float, true>(p, st, dev, nsm)
+             : launch_all<float, false>(p, st, dev, nsm);
+}
+
+}  // namespace
+}  // namespace sv
+
+extern "C" {
+
+size_t sv_workspace_bytes(int B, int gamma_max, int V) {
+  if (!sv::sizes_ok(B, gamma_max, V)) return 0;
+  return sv::make_layout(B, gamma_max, V).total;
+}
+
+sv_status spec_verify(const void *target_logits, sv_dtype logits_dtype,
+                      const int32_t *draft_token_ids, const float *draft_probs,
+                      const float *uniforms_accept, const float *uniforms_sample,
+                      const float *temperature, const int32_t *draft_lens, int B,
+                      int gamma_max, int V, int32_t *out_tokens, int32_t *out_num_accepted,
+                      void *workspace, size_t workspace_bytes, sv_stream_t stream) {
+  return sv::run(target_logits, logits_dtype, draft_token_ids, draft_probs, uniforms_accept,
+                 uniforms_sample, temperature, draft_lens, B, gamma_max, V, out_tokens,
+                 out_num_accepted, workspace, workspace_bytes, stream, nullptr);
+}
+
+sv_status spec_verify_diag(const void *target_logits, sv_dtype logits_dtype,
+                           const int32_t *draft_token_ids, const float *draft_probs,
+                           const float *uniforms_accept, const float *uniforms_sample,
+                           const float *temperature, const int32_t *draft_lens, int B,
+                           int gamma_max, int V, int32_t *out_tokens,
+                           int32_t *out_num_accepted, void *workspace,
+                           size_t workspace_bytes, sv_stream_t stream, const sv_diag *diag) {
+  return sv::run(target_logits, logits_dtype, draft_token_ids, draft_probs, uniforms_accept,
+                 uniforms_sample, temperature, draft_lens, B, gamma_max, V, out_tokens,
+                 out_num_accepted, workspace, workspace_bytes, stream, diag);
+}
+
+sv_status sv_last_error(const void *workspace, sv_stream_t stream, uint32_t *out_word) {
+  if (!workspace) return SV_ERR_INVALID_ARG;
+  uint32_t word = 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const auto *hdr = static_cast<const sv::Header *>(workspace);
+  if (cudaMemcpyAsync(&word, &hdr->err, sizeof word, cudaMemcpyDeviceToHost, st) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (out_word) *out_word = word;
+  if (word & SV_FAULT_TIMEOUT) return SV_ERR_TIMEOUT;
+  if (word) return SV_ERR_BAD_INPUT_DATA;
+  return SV_OK;
+}
+
+const char *sv_status_string(sv_status status) {
+  switch (status) {
+    case SV_OK: return "SV_OK";
+    case SV_ERR_INVALID_ARG: return "SV_ERR_INVALID_ARG: invalid argument";
+    case SV_ERR_UNSUPPORTED_DTYPE: return "SV_ERR_UNSUPPORTED_DTYPE: logits dtype not fp32/bf16";
+    case SV_ERR_WORKSPACE_TOO_SMALL: return "SV_ERR_WORKSPACE_TOO_SMALL: workspace too small";
+    case SV_ERR_CUDA: return "SV_ERR_CUDA: CUDA runtime call or launch failed";
+    case SV_ERR_TIMEOUT: return "SV_ERR_TIMEOUT: a bounded device wait gave up";
+    case SV_ERR_BAD_INPUT_DATA: return "SV_ERR_BAD_INPUT_DATA: a request had invalid data";
+  }
+  return "unknown sv_status";
+}
+
+}  // extern "C"

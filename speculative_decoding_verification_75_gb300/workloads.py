@@ -124,7 +124,7 @@ def make_case(w: Workload, device="cpu", seed: Optional[int] = None,
     # Draft distributions: noisy copies of the (rounded) target rows.
     ids = torch.empty(B, g, device=device, dtype=torch.int32)
     q_all = torch.empty(B, g, V, **f32) if draft_probs else None
-    for b in range(B):
+    for b in range(B if g > 0 else 0):
         d = logits[b, :g].float() + noise[b] * torch.randn(g, V, generator=gen, **f32)
         T = float(temperature[b])
         if T > 0:
