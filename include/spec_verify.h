@@ -169,6 +169,48 @@ SV_API sv_status sv_last_error(const void *workspace, sv_stream_t stream,
 /* Static, human-readable name of a status code. */
 SV_API const char *sv_status_string(sv_status status);
 
+/*
+ * Allocation-free variant of spec_verify.  The tutorial page has no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory -- code running inside a CUDA-graph-driven or real-time
+ * serving loop that forbids allocation on its hot path, plugins handed a
+ * device context but no allocator, or C callers without a CUDA memory
+ * manager -- and so cannot provide the workspace spec_verify needs.
+ *
+ * Instead of a caller-provided workspace it uses one scratch array of
+ * SV_NOALLOC_SCRATCH_BYTES bytes that the library defines in device memory
+ * (a file-scope __device__ array: every GPU that loads the library keeps it
+ * until the process exits).  Everything else -- inputs, outputs, stream,
+ * results -- is as for spec_verify.
+ *
+ *   - Sizes whose workspace, sv_workspace_bytes(B, gamma_max, V), exceeds
+ *     SV_NOALLOC_SCRATCH_BYTES are rejected with SV_ERR_WORKSPACE_TOO_SMALL
+ *     before anything is enqueued (B=256, gamma_max=7, V=151936 needs about
+ *     1 MiB).
+ *   - The first call on a device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before capturing any stream on the device.
+ *   - Every call on a device shares the one array, and each call resets what
+ *     must start at zero; calls whose work may overlap on the GPU (other
+ *     streams, other host threads) race on it and must be serialised by the
+ *     caller, e.g. by issuing them on one stream.
+ *   - Invalid per-request data is reported through out_num_accepted = -1
+ *     (the error word of sv_last_error lives in the scratch array and is not
+ *     exposed).
+ *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library
+ *     call is made.
+ */
+#define SV_NOALLOC_SCRATCH_BYTES (4u << 20)
+SV_API sv_status spec_verify_noalloc(const void *target_logits, sv_dtype logits_dtype,
+                                     const int32_t *draft_token_ids,
+                                     const float *draft_probs,
+                                     const float *uniforms_accept,
+                                     const float *uniforms_sample,
+                                     const float *temperature,
+                                     const int32_t *draft_lens, int B, int gamma_max,
+                                     int V, int32_t *out_tokens,
+                                     int32_t *out_num_accepted, sv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

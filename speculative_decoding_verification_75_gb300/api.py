@@ -37,7 +37,7 @@ SV_FAULT_TIMEOUT = 0x10000
 
 # Every symbol include/spec_verify.h declares.
 EXPORTS = ("sv_workspace_bytes", "spec_verify", "spec_verify_diag",
-           "sv_last_error", "sv_status_string")
+           "sv_last_error", "sv_status_string", "spec_verify_noalloc")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int

@@ -215,4 +215,48 @@ const char *sv_status_string(sv_status status) {
   return "unknown sv_status";
 }
 
+// ------------------------------------------------ allocation-free variant ----
+// For callers that cannot allocate device memory: the workspace lives in one
+// file-scope device array instead of caller memory.  Host code never uses the
+// array's name as an address (on the host it is only a stand-in symbol); its
+// device address is looked up once per device with cudaGetSymbolAddress.
+
+namespace {
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SV_NOALLOC_SCRATCH_BYTES];
+std::atomic<void *> g_noalloc_addr[sv::kMaxDevices];
+
+// Device address of the scratch array on the current device (looked up on
+// the first call per device, that device being current).
+sv_status noalloc_scratch(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= sv::kMaxDevices) return SV_ERR_CUDA;
+  void *ptr = g_noalloc_addr[dev].load(std::memory_order_acquire);
+  if (!ptr) {
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return SV_ERR_CUDA;
+    g_noalloc_addr[dev].store(ptr, std::memory_order_release);
+  }
+  *out = ptr;
+  return SV_OK;
+}
+}  // namespace
+
+sv_status spec_verify_noalloc(const void *target_logits, sv_dtype logits_dtype,
+                              const int32_t *draft_token_ids, const float *draft_probs,
+                              const float *uniforms_accept, const float *uniforms_sample,
+                              const float *temperature, const int32_t *draft_lens, int B,
+                              int gamma_max, int V, int32_t *out_tokens,
+                              int32_t *out_num_accepted, sv_stream_t stream) {
+  if (logits_dtype != SV_F32 && logits_dtype != SV_BF16) return SV_ERR_UNSUPPORTED_DTYPE;
+  if (!sv::sizes_ok(B, gamma_max, V)) return SV_ERR_INVALID_ARG;
+  if (sv::make_layout(B, gamma_max, V).total > SV_NOALLOC_SCRATCH_BYTES)
+    return SV_ERR_WORKSPACE_TOO_SMALL;
+  if (B == 0) return SV_OK;
+  void *scratch = nullptr;
+  const sv_status st = noalloc_scratch(&scratch);
+  if (st != SV_OK) return st;
+  return sv::run(target_logits, logits_dtype, draft_token_ids, draft_probs, uniforms_accept,
+                 uniforms_sample, temperature, draft_lens, B, gamma_max, V, out_tokens,
+                 out_num_accepted, scratch, SV_NOALLOC_SCRATCH_BYTES, stream, nullptr);
+}
+
 }  // extern "C"
