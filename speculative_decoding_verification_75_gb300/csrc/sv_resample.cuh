@@ -423,26 +423,29 @@ __global__ void __launch_bounds__(K2Shape<T>::kThreads, 1) sv_resample_kernel(Pa
     if (lane != 0) return;
     // ------------------------------------------------ producer lane ----
     const uint64_t pol_l = policy_evict_normal(), pol_q = policy_evict_first();
-    const long long nq = ld_cg(&p.hdr->n_q), nn = ld_cg(&p.hdr->n_noq);
-    const long long C = p.C2, total = (nq + nn) * C;
-    long long n = 0, cur = -1;
+    // 32-bit item arithmetic (item counts are below B * C2 < 2^31): this lane
+    // issues every copy of the CTA and must stay cheap.
+    const int nq = static_cast<int>(ld_cg(&p.hdr->n_q)), nn = static_cast<int>(ld_cg(&p.hdr->n_noq));
+    const int C = p.C2, total = (nq + nn) * C;
+    uint32_t n = 0;
+    int cur = -1;
     Desc d{};
     bool ok = true;
     // Item indices come from a global counter; the next one is requested
     // while the current one is issued, hiding the atomic's latency.
-    long long it = atomicAdd(&p.hdr->k2_next, 1u);
+    int it = static_cast<int>(atomicAdd(&p.hdr->k2_next, 1u));
     while (it < total) {
-      const long long nxt = atomicAdd(&p.hdr->k2_next, 1u);
-      const bool hq = it < nq * C;
-      const long long li = hq ? it / C : nq + (it - nq * C) / C;
-      const int c = static_cast<int>(hq ? it % C : (it - nq * C) % C);
+      const int nxt = static_cast<int>(atomicAdd(&p.hdr->k2_next, 1u));
+      const int li = it / C;  // rows that read q come first in the item order
+      const int c = it - li * C;
+      const bool hq = li < nq;
       if (li != cur) {
         d = ld_cg(hq ? p.desc_q + li : p.desc_noq + (li - nq));
         cur = li;
       }
       const int e0 = c * S::kChunk, ne = min(S::kChunk, p.V - e0);
       const int s = static_cast<int>(n % S::kStages);
-      const uint32_t ph = static_cast<uint32_t>((n / S::kStages) & 1);
+      const uint32_t ph = (n / S::kStages) & 1u;
       if (n >= S::kStages && !(ok = mbar_wait(empty0 + 8 * s, ph ^ 1u, err))) break;
       info[s] = ItemInfo2{d, c, ne, hq ? 1 : 0, 0};
       if (kTMA) {
@@ -470,7 +473,7 @@ __global__ void __launch_bounds__(K2Shape<T>::kThreads, 1) sv_resample_kernel(Pa
       info[s].c = -1;
       mbar_arrive(full0 + 8 * s);
     }
-    for (long long j = (n > S::kStages ? n - S::kStages : 0); j < n; ++j)
+    for (uint32_t j = (n > S::kStages ? n - S::kStages : 0); j < n; ++j)
       mbar_wait(full0 + 8 * static_cast<int>(j % S::kStages),
                 static_cast<uint32_t>((j / S::kStages) & 1), err);
     return;
@@ -478,7 +481,7 @@ __global__ void __launch_bounds__(K2Shape<T>::kThreads, 1) sv_resample_kernel(Pa
 
   // ---------------------------------------------------- consumer warps ----
   const int cw = warp - 1;
-  for (long long n = cw;; n += S::kConsumers) {
+  for (uint32_t n = cw;; n += S::kConsumers) {
     const int s = static_cast<int>(n % S::kStages);
     const uint32_t ph = static_cast<uint32_t>((n / S::kStages) & 1);
     if (!mbar_wait(full0 + 8 * s, ph, err)) break;

@@ -494,7 +494,7 @@ __global__ void __launch_bounds__(kK1Threads, 1) sv_rowstats_kernel(Params p) {
     if (lane != 0) return;
     // ------------------------------------------------ producer lane ----
     const uint64_t pol = policy_evict_normal();
-    long long n = 0;
+    uint32_t n = 0;
     bool ok = true;
     if (lo < hi) {
       int b = s_b0, rs = s_rs0, j = 0;
@@ -502,9 +502,10 @@ __global__ void __launch_bounds__(kK1Threads, 1) sv_rowstats_kernel(Params p) {
       float cs = 0.f;
       int ltotal = 0, gtotal = 0;
       bool fresh = true;
-      for (long long it = lo; it < hi; ++it, ++n) {
-        const long long fr = it / p.C;
-        const int c = static_cast<int>(it % p.C);
+      // (row, chunk) advanced incrementally: this lane issues every copy of
+      // the CTA, and a 64-bit division per item would make it the bottleneck.
+      int fr = static_cast<int>(lo / p.C), c = static_cast<int>(lo - static_cast<long long>(fr) * p.C);
+      for (long long it = lo; it < hi; ++it, ++n, (++c == p.C ? (c = 0, ++fr) : 0)) {
         while (fr >= rs + nr) {  // next request with rows
           rs += nr;
           ++b;
@@ -521,10 +522,10 @@ __global__ void __launch_bounds__(kK1Threads, 1) sv_rowstats_kernel(Params p) {
           if (it != lo) ++j;
           fresh = false;
         }
-        const int slot = b * R + static_cast<int>(fr - rs);
+        const int slot = b * R + (fr - rs);
         const int e0 = c * kChunk, ne = min(kChunk, p.V - e0);
         const int s = static_cast<int>(n % kK1Stages);
-        const uint32_t ph = static_cast<uint32_t>((n / kK1Stages) & 1);
+        const uint32_t ph = (n / kK1Stages) & 1u;
         if (n >= kK1Stages && !(ok = mbar_wait(empty0 + 8 * s, ph ^ 1u, err))) break;
         info[s] = ItemInfo{slot, c, ne, cs, b, j % kLocalSlots, ltotal, gtotal};
         if (kTMA) {
@@ -546,7 +547,7 @@ __global__ void __launch_bounds__(kK1Threads, 1) sv_rowstats_kernel(Params p) {
       mbar_arrive(full0 + 8 * s);
     }
     // Every copy this CTA issued must have landed before it exits.
-    for (long long jj = (n > kK1Stages ? n - kK1Stages : 0); jj < n; ++jj)
+    for (uint32_t jj = (n > kK1Stages ? n - kK1Stages : 0); jj < n; ++jj)
       mbar_wait(full0 + 8 * static_cast<int>(jj % kK1Stages),
                 static_cast<uint32_t>((jj / kK1Stages) & 1), err);
     return;
@@ -559,7 +560,7 @@ __global__ void __launch_bounds__(kK1Threads, 1) sv_rowstats_kernel(Params p) {
   // later, so all of the previous owner's items are counted by then.
   const int cw = warp - 1;
   bool waited = false;
-  for (long long n = cw;; n += kK1Consumers) {
+  for (uint32_t n = cw;; n += kK1Consumers) {
     const int s = static_cast<int>(n % kK1Stages);
     const uint32_t ph = static_cast<uint32_t>((n / kK1Stages) & 1);
     if (!mbar_wait(full0 + 8 * s, ph, err)) break;
