@@ -1,15 +1,17 @@
 // spec_verify.cu -- C ABI of the GB300 speculative-decoding verification
-// library: argument checks, workspace carving and the three launches.
+// library: argument checks, workspace carving and the two launches.
 //
-//   kernel 0  sv_prepare_kernel    reset per-call counters, reject bad lengths
-//   kernel 1  sv_rowstats_kernel   softmax statistics of every row, accept
-//                                  test and first rejection per request
-//   kernel 2  sv_resample_kernel   residual / bonus draw for sampled requests
+//   kernel 0  sv_prepare_kernel  per-request row offsets and softmax scales,
+//                                reset of the per-call counters, rejection of
+//                                bad draft lengths
+//   kernel 1  sv_verify_kernel   persistent: softmax statistics of every row,
+//                                accept test and first rejection per request,
+//                                residual / bonus draw for sampled requests
 //
-// Kernels 1 and 2 are launched with programmatic stream serialisation so
-// that each one's launch and prologue overlap the tail of its predecessor.
-// Each of them comes in a TMA variant (rows start on 16-byte boundaries) and
-// a plain-load variant for any other alignment.
+// Kernel 1 is launched with programmatic stream serialisation so that its
+// launch and prologue overlap kernel 0.  It comes in a TMA variant (rows
+// start on 16-byte boundaries) and a plain-load variant for any other
+// alignment.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -20,8 +22,7 @@
 #include "sv_device.cuh"
 #include "sv_layout.cuh"
 #include "sv_prepare.cuh"
-#include "sv_resample.cuh"
-#include "sv_rowstats.cuh"
+#include "sv_verify.cuh"
 
 namespace sv {
 namespace {
@@ -67,31 +68,21 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
 
 template <typename T, bool kTMA>
 sv_status launch_all(Params &p, cudaStream_t st, int dev, int nsm) {
-  static std::atomic<uint64_t> k1_done{0}, k2_done{0};
-  constexpr int kChunk = Elem<T>::kChunk;
-  p.C = div_up(p.V, kChunk);
-  p.C2 = div_up(p.V, kK2Chunk);
-  p.nseg = div_up(p.V, kSeg);
+  static std::atomic<uint64_t> smem_done{0};
+  p.C1 = div_up(p.V, Tiling<T>::kRowChunk);
+  p.C2 = div_up(p.V, Tiling<T>::kResChunk);
+  p.nseg = p.C2 * Tiling<T>::kSegPerChunk;
 
-  auto *k1 = sv_rowstats_kernel<T, kTMA>;
-  auto *k2 = sv_resample_kernel<T, kTMA>;
-  const size_t s1 = k1_smem_bytes();
-  const size_t s2 = k2_smem_bytes<T>(kTMA);
-  if (ensure_smem(k1, s1, k1_done, dev) != cudaSuccess ||
-      ensure_smem(k2, s2, k2_done, dev) != cudaSuccess)
-    return SV_ERR_CUDA;
+  auto *kv = sv_verify_kernel<T, kTMA>;
+  const size_t smem = verify_smem_bytes();
+  if (ensure_smem(kv, smem, smem_done, dev) != cudaSuccess) return SV_ERR_CUDA;
 
   sv_prepare_kernel<<<1, kPrepThreads, 0, st>>>(p);
   if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
 
-  const long long max_items = static_cast<long long>(p.B) * (p.gmax + 1) * p.C;
-  const int g1 = static_cast<int>(max_items < nsm ? max_items : nsm);
-  if (launch_pdl(k1, dim3(g1), dim3(kK1Threads), s1, st, p) != cudaSuccess)
-    return SV_ERR_CUDA;
-
-  const long long max_items2 = static_cast<long long>(p.B) * p.C2;
-  const int g2 = static_cast<int>(max_items2 < nsm ? max_items2 : nsm);
-  if (launch_pdl(k2, dim3(g2), dim3(K2Shape<T>::kThreads), s2, st, p) != cudaSuccess)
+  const long long max_items = static_cast<long long>(p.B) * (p.gmax + 1) * p.C1;
+  const int grid = static_cast<int>(max_items < nsm ? max_items : nsm);
+  if (launch_pdl(kv, dim3(grid), dim3(kThreads), smem, st, p) != cudaSuccess)
     return SV_ERR_CUDA;
   return SV_OK;
 }
@@ -134,10 +125,13 @@ sv_status run(const void *logits, sv_dtype dtype, const int32_t *ids, const floa
   p.out_nacc = out_nacc;
   if (diag) p.diag = *diag;
   p.hdr = reinterpret_cast<Header *>(w + L.hdr);
+  p.row_start = reinterpret_cast<int *>(w + L.row_start);
+  p.cs = reinterpret_cast<float *>(w + L.cs);
   p.k1_cnt = reinterpret_cast<uint32_t *>(w + L.k1_cnt);
   p.k2_cnt = reinterpret_cast<uint32_t *>(w + L.k2_cnt);
-  p.desc_q = reinterpret_cast<Desc *>(w + L.desc_q);
-  p.desc_noq = reinterpret_cast<Desc *>(w + L.desc_noq);
+  p.ready = reinterpret_cast<uint32_t *>(w + L.ready);
+  p.desc = reinterpret_cast<Desc *>(w + L.desc);
+  p.jflag = reinterpret_cast<uint32_t *>(w + L.jflag);
   p.part1 = reinterpret_cast<Part *>(w + L.part1);
   p.csum = reinterpret_cast<float2 *>(w + L.csum);
   p.ssum = reinterpret_cast<float2 *>(w + L.ssum);

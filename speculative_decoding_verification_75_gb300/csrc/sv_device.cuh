@@ -50,6 +50,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of a phase (try_wait may suspend the thread for a while;
+// test_wait returns at once).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; "
+      "selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -102,6 +115,47 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const void *src,
       : "memory");
 }
 
+// Whole-warp wait on an mbarrier phase; false (for every lane) on timeout.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint32_t *err) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
+}
+
+// ------------------------------------------------------- smem queues ----
+// Single-producer single-consumer queue in shared memory: N entries of type
+// E, each slot guarded by a "full" and an "empty" mbarrier (count 1).  One
+// carries claimed work from a CTA's claimer lane to its producer lane, one
+// carries completed runs from the producer lane to the service warp (so that
+// merges and searches, several dependent memory round trips, never stall the
+// streaming pipeline).
+constexpr int kSvcSlots = 32;
+
+template <typename E, int N = kSvcSlots>
+struct SvcQueue {
+  static constexpr int kSlots = N;
+  E slot[N];
+  uint64_t full[N];
+  uint64_t empty[N];
+};
+
+template <typename Q>
+__device__ __forceinline__ void svc_init(Q *q) {
+  for (int i = 0; i < Q::kSlots; ++i) {
+    mbar_init(smem_addr(&q->full[i]), 1);
+    mbar_init(smem_addr(&q->empty[i]), 1);
+  }
+}
+
+// Producer side (one thread), entry number k.  False on timeout.
+template <typename Q, typename E>
+__device__ __forceinline__ bool svc_push(Q *q, uint32_t k, const E &e, uint32_t *err) {
+  constexpr uint32_t N = Q::kSlots;
+  const int i = static_cast<int>(k % N);
+  if (k >= N && !mbar_wait(smem_addr(&q->empty[i]), ((k / N) & 1u) ^ 1u, err)) return false;
+  q->slot[i] = e;
+  mbar_arrive(smem_addr(&q->full[i]));  // release: the entry and all the pusher observed
+  return true;
+}
+
 // Programmatic dependent launch: wait for the preceding grid's completion
 // (and memory flush), and allow the next grid to start its prologue.
 __device__ __forceinline__ void pdl_wait() {
@@ -130,7 +184,6 @@ struct Elem;
 
 template <>
 struct Elem<float> {
-  static constexpr int kChunk = 4096;  // elements per 16 KiB chunk
   __device__ __forceinline__ static float load(const float *p, size_t i) {
     return __ldg(p + i);
   }
@@ -138,7 +191,6 @@ struct Elem<float> {
 
 template <>
 struct Elem<__nv_bfloat16> {
-  static constexpr int kChunk = 8192;
   __device__ __forceinline__ static float load(const __nv_bfloat16 *p, size_t i) {
     const unsigned short h = __ldg(reinterpret_cast<const unsigned short *>(p) + i);
     return __uint_as_float(static_cast<uint32_t>(h) << 16);
@@ -184,6 +236,40 @@ __device__ __forceinline__ uint32_t atomic_add_acq_rel(uint32_t *p, uint32_t v) 
                : "l"(p), "r"(v)
                : "memory");
   return old;
+}
+
+__device__ __forceinline__ void st_release(uint32_t *p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed(uint32_t *p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_add_release(uint32_t *p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Orders this thread's earlier loads (that observed other threads' writes)
+// before its later accesses, at device scope.
+__device__ __forceinline__ void fence_acq_rel() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Two adjacent 32-bit counters read in one access (8-byte aligned).
+__device__ __forceinline__ uint2 ld_relaxed2(const uint32_t *p) {
+  uint2 v;
+  asm volatile("ld.relaxed.gpu.global.v2.u32 {%0, %1}, [%2];"
+               : "=r"(v.x), "=r"(v.y)
+               : "l"(p)
+               : "memory");
+  return v;
 }
 
 // Loads that bypass L1 (data written by other CTAs of the same grid), for

@@ -1,11 +1,12 @@
-// sv_prepare.cuh -- kernel 0: reset the workspace's counters for this call.
+// sv_prepare.cuh -- kernel 0: per-call set-up of the workspace.
 //
-// One CTA clears the per-request arrival counters and the header, and writes
-// the -1 outputs of requests whose draft length is invalid (they have no rows
-// for the row-statistics kernel to stream).  Every other per-request check
-// happens in the row-statistics kernel's merge step.  The row-statistics
-// kernel streams logits while this runs; it waits for this grid only before
-// its first counter update.
+// One CTA walks the batch 1024 requests at a time: it writes each request's
+// first flat row (an exclusive scan of g_b + 1) and softmax scale log2(e)/T,
+// clears the request's arrival counters and descriptor flag, and writes the
+// -1 outputs of requests whose draft length is invalid (they get no rows).
+// Every other per-request check happens in the merge step.  It also resets
+// the header: error word, row and request totals, and the work counters of
+// the persistent kernel.
 #pragma once
 
 #include "sv_device.cuh"
@@ -38,24 +39,73 @@ __device__ void fill_bad_request(const Params &p, int b) {
 }
 
 __global__ void __launch_bounds__(kPrepThreads) sv_prepare_kernel(Params p) {
+  // The persistent kernel may start its prologue now; it waits for this
+  // grid's completion before it reads anything written here.
   pdl_launch_dependents();
+  __shared__ int warp_tot[32];
+  __shared__ int carry, valid;
   __shared__ uint32_t err_acc;
-  if (threadIdx.x == 0) err_acc = 0;
-  __syncthreads();
-  for (int b = threadIdx.x; b < p.B; b += kPrepThreads) {
-    p.k1_cnt[b] = 0u;
-    p.k2_cnt[b] = 0u;
-    if (request_rows(p, b) == 0) {
-      fill_bad_request(p, b);
-      atomicOr(&err_acc, SV_BAD_DRAFT_LEN);
-    }
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    carry = 0;
+    valid = 0;
+    err_acc = 0;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  for (int base = 0; base < p.B; base += kPrepThreads) {
+    const int b = base + tid;
+    int nr = 0;
+    if (b < p.B) {
+      nr = request_rows(p, b);
+      const float t = __ldg(p.temp + b);
+      p.cs[b] = (t > 0.f) ? kLog2e / t : 0.f;
+      p.k1_cnt[b] = 0u;
+      p.k2_cnt[b] = 0u;
+      p.ready[b] = kPending;
+      p.jflag[b] = nr == 0 ? kJobNone : kJobWait;  // no merge without rows
+      p.jflag[p.B + b] = kJobWait;
+      if (nr == 0) {
+        fill_bad_request(p, b);
+        atomicOr(&err_acc, SV_BAD_DRAFT_LEN);
+      } else {
+        atomicAdd(&valid, 1);
+      }
+    }
+    // Exclusive scan of the row counts: first flat row of each request.
+    int incl = nr;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_tot[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(kFull, w, o);
+        if (lane >= o) w += n;
+      }
+      warp_tot[lane] = w;
+    }
+    __syncthreads();
+    if (b < p.B) p.row_start[b] = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + incl - nr;
+    __syncthreads();
+    if (tid == 0) carry += warp_tot[31];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    p.row_start[p.B] = carry;
     p.hdr->err = err_acc;
-    p.hdr->n_q = 0u;
-    p.hdr->n_noq = 0u;
-    p.hdr->k2_next = 0u;
+    p.hdr->n_rows = static_cast<uint32_t>(carry);
+    p.hdr->n_valid = static_cast<uint32_t>(valid);
+    p.hdr->a_next = 0u;
+    p.hdr->b_next = 0u;
+    p.hdr->b_reserved = 0u;
+    p.hdr->n_merged = 0u;
+    p.hdr->jq_head = 0u;
+    p.hdr->all_merged = valid == 0 ? 1u : 0u;  // nothing to merge
   }
 }
 

@@ -1,5 +1,5 @@
-// sv_resample.cuh -- kernel 2: the residual re-sample at the first rejection
-// and the bonus draw when every draft was kept.
+// sv_resample.cuh -- the residual (or bonus) sums of one chunk, and the
+// inverse-CDF search of a request.
 //
 // Tutorial page dpshk.com/news/5598276 (HTML title 企业官网建设流程全解析):
 // §3.1 step 4 and §5.2 step (5) (_recover_rejected): r = (p_k - q_k)_+,
@@ -7,76 +7,18 @@
 // page's multinomial draw becomes an inverse-CDF draw on the caller's uniform:
 // token = min{ j : C_j > u * S }, C the inclusive prefix sum of r, S = C_V.
 //
-// Only the rows kernel 1 queued are read: one logits row per sampled request
-// and, at a rejection, the draft's q row at that position.  Items are
-// (request, 4096-element chunk) pairs handed out one at a time from a global
-// counter (rows that read q first), so CTAs stay busy whatever mix of
-// rejections and bonus draws a batch has.  A producer lane streams each chunk
-// (logits + q) into a shared-memory stage with 1-D TMA bulk copies, and a
-// consumer warp forms p and (p - q)_+ on the fly with packed fp32x2
-// arithmetic, recording the sums of every 1024-element segment.  The last
-// chunk of a request to finish walks chunk sums, then segment sums, then the
-// elements of one segment to find the token: a three-level inverse-CDF search
-// that re-reads 1024 elements instead of the whole row.
+// Only the row each sampled request draws from is re-read, and q only at a
+// rejection.  A consumer warp forms p and (p - q)_+ on the fly with packed
+// fp32x2 arithmetic and records the sums of every 1024-element segment; when
+// every chunk of the request is done, one warp walks chunk sums, segment sums
+// and then the elements of one segment to find the token: a three-level
+// search that re-reads 1024 elements instead of the whole row.
 #pragma once
 
 #include "sv_device.cuh"
 #include "sv_layout.cuh"
 
 namespace sv {
-
-// Pipeline shape per logits dtype (stage = logits chunk + q chunk), one stage
-// per consumer warp: on GB300 more reducing warps beat deeper buffering.
-#ifndef SV_K2_BF16_CONSUMERS
-#define SV_K2_BF16_CONSUMERS 8
-#endif
-#ifndef SV_K2_BF16_STAGES
-#define SV_K2_BF16_STAGES 8
-#endif
-#ifndef SV_K2_F32_CONSUMERS
-#define SV_K2_F32_CONSUMERS 6
-#endif
-#ifndef SV_K2_F32_STAGES
-#define SV_K2_F32_STAGES 6
-#endif
-template <typename T>
-struct K2Cfg;
-template <>
-struct K2Cfg<__nv_bfloat16> {
-  static constexpr int kStages = SV_K2_BF16_STAGES, kConsumers = SV_K2_BF16_CONSUMERS;
-};
-template <>
-struct K2Cfg<float> {
-  static constexpr int kStages = SV_K2_F32_STAGES, kConsumers = SV_K2_F32_CONSUMERS;
-};
-
-template <typename T>
-struct K2Shape {
-  static constexpr int kChunk = kK2Chunk;
-  static constexpr int kLBytes = kChunk * static_cast<int>(sizeof(T));
-  static constexpr int kQBytes = kChunk * 4;
-  static constexpr int kStageBytes = kLBytes + kQBytes;
-  static constexpr int kStages = K2Cfg<T>::kStages;
-  static constexpr int kConsumers = K2Cfg<T>::kConsumers;
-  static constexpr int kThreads = 32 * (kConsumers + 1);
-  static constexpr int kSegPerChunk = kChunk / kSeg;
-  static_assert(kStages % kConsumers == 0, "each consumer warp owns whole stages");
-};
-
-struct ItemInfo2 {
-  Desc d;
-  int c;      // chunk (-1: end of stream)
-  int ne;
-  int has_q;
-  int pad;
-};
-
-template <typename T>
-constexpr size_t k2_smem_bytes(bool tma) {
-  using S = K2Shape<T>;
-  return (tma ? static_cast<size_t>(S::kStages) * S::kStageBytes : 0) +
-         S::kStages * sizeof(ItemInfo2) + 2 * S::kStages * sizeof(uint64_t);
-}
 
 // p_j of the target softmax and r_j = (p_j - q_j)_+, as a fixed sequence of
 // correctly rounded operations: the packed fp32x2 forms in the streaming pass
@@ -247,11 +189,91 @@ __device__ __forceinline__ int search_segment(const Params &p, const Desc &d, in
   return e0 + 32 * src + __shfl_sync(kFull, lastpos, src);
 }
 
-// Last arriver of a request: walk chunk sums, segment sums, then elements.
+// Inverse-CDF walk over n <= 256 weights held eight per lane, lane l owning
+// indices 8l..8l+7 in order: the first index whose inclusive prefix exceeds
+// target, else the last index with positive weight (then *fell_back is set).
+// Also returns the exclusive prefix at that index.
+__device__ __forceinline__ int cdf_block8(int n, const float (&w)[8], float target, int lane,
+                                          float *excl_out, bool *fell_back) {
+  float tot = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) tot += (8 * lane + j < n) ? w[j] : 0.f;
+  const float incl = warp_inclusive_scan(tot, lane);
+  const float prev = __shfl_up_sync(kFull, incl, 1);
+  float c = (lane == 0) ? 0.f : prev;  // this lane's starting prefix
+  int hit = -1, lastpos = -1;
+  float hit_excl = 0.f, last_excl = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const bool in = 8 * lane + j < n;
+    const float wj = in ? w[j] : 0.f;
+    if (in && hit < 0 && c + wj > target) {
+      hit = j;
+      hit_excl = c;
+    }
+    if (in && wj > 0.f) {
+      lastpos = j;
+      last_excl = c;
+    }
+    c += wj;
+  }
+  const unsigned hb = __ballot_sync(kFull, hit >= 0);
+  if (hb) {
+    const int src = __ffs(hb) - 1;
+    *excl_out = __shfl_sync(kFull, hit_excl, src);
+    return 8 * src + __shfl_sync(kFull, hit, src);
+  }
+  *fell_back = true;
+  const unsigned pb = __ballot_sync(kFull, lastpos >= 0);
+  if (!pb) {
+    *excl_out = 0.f;
+    return -1;
+  }
+  const int src = 31 - __clz(pb);
+  *excl_out = __shfl_sync(kFull, last_excl, src);
+  return 8 * src + __shfl_sync(kFull, lastpos, src);
+}
+
+// Draw of descriptor slot sl (row d), once every chunk of its residual is
+// reduced.  Rows of up to 256 segments: one wave of loads fetches every
+// segment sum, a walk over them finds the segment, a second wave fetches its
+// elements.  Longer rows walk chunk sums, segment sums, then elements.
 template <typename T, bool kVec>
-__device__ void search_request(const Params &p, const Desc &d, int lane) {
-  const float2 *cs2 = p.csum + static_cast<size_t>(d.b) * p.C2;
-  const float2 *ss2 = p.ssum + static_cast<size_t>(d.b) * p.nseg;
+__device__ void search_request(const Params &p, const Desc &d, int sl, int lane) {
+  const float2 *cs2 = p.csum + static_cast<size_t>(sl) * p.C2;
+  const float2 *ss2 = p.ssum + static_cast<size_t>(sl) * p.nseg;
+  const int nsr = (p.V + kSeg - 1) / kSeg;  // segments of the row
+  if (nsr <= 256) {
+    float wr[8], wp[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = 8 * lane + j;
+      const float2 v = (i < nsr) ? ld_cg(ss2 + i) : make_float2(0.f, 0.f);
+      wr[j] = v.x;
+      wp[j] = v.y;
+    }
+    float lr = 0.f, lp = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      lr += wr[j];
+      lp += wp[j];
+    }
+    const float tr = __shfl_sync(kFull, warp_inclusive_scan(lr, lane), 31);
+    const float tp = __shfl_sync(kFull, warp_inclusive_scan(lp, lane), 31);
+    const bool use_p = !(tr > 0.f);  // empty residual: draw from p itself
+    float target = __fmul_rn(d.u, use_p ? tp : tr);
+    bool fb = false;
+    float base = 0.f;
+    const int sg = max(0, cdf_block8(nsr, use_p ? wp : wr, target, lane, &base, &fb));
+    if (fb) target = INFINITY;  // rounding pushed u*S past the total
+    const int j = search_segment<T, kVec>(p, d, sg * kSeg, min(kSeg, p.V - sg * kSeg), base,
+                                          target, use_p, lane);
+    if (lane == 0) {
+      p.out_tokens[static_cast<size_t>(d.b) * (p.gmax + 1) + d.k] = j;
+      if (p.diag.resid_mass) p.diag.resid_mass[d.b] = tr;
+    }
+    return;
+  }
 
   // Totals of the residual and of p, in the same scan order the walk uses.
   float tr = 0.f, tp = 0.f;
@@ -293,8 +315,9 @@ __device__ void search_request(const Params &p, const Desc &d, int lane) {
   }
   c = max(0, c);
   if (fb) target = INFINITY;  // rounding pushed u*S past the total
-  const int g0 = c * K2Shape<T>::kSegPerChunk;
-  const int nsg = (min(kK2Chunk, p.V - c * kK2Chunk) + kSeg - 1) / kSeg;
+  constexpr int kChunk = Tiling<T>::kResChunk;
+  const int g0 = c * Tiling<T>::kSegPerChunk;
+  const int nsg = (min(kChunk, p.V - c * kChunk) + kSeg - 1) / kSeg;
   float2 sv = make_float2(0.f, 0.f);
   if (lane < nsg) sv = ld_cg(ss2 + g0 + lane);
   float base2 = 0.f;
@@ -311,31 +334,34 @@ __device__ void search_request(const Params &p, const Desc &d, int lane) {
 
 // ------------------------------------------------------ chunk residual ----
 
-// Residual and p sums of one chunk per 1024-element segment.  Lane layout:
-// each 256-element step gives lane l the elements 4l..4l+3 and
+// Residual and p sums of one chunk per 1024-element segment, for the
+// segments h, h + 2, ... of the chunk (two warps share a chunk).  Writes the
+// segment sums and returns this warp's share of the chunk sums (in lane 0).
+// Lane layout: each 256-element step gives lane l the elements 4l..4l+3 and
 // 128+4l..128+4l+3 (conflict-free 8- and 16-byte shared-memory reads).
 template <typename T, bool kTMA>
-__device__ __forceinline__ void chunk_resid(const Params &p, const ItemInfo2 &inf,
-                                            const uint8_t *stage, int lane) {
-  const Desc &d = inf.d;
-  const int e0 = inf.c * kK2Chunk;
+__device__ __forceinline__ float2 chunk_resid(const Params &p, const Desc &d, int sl, int chunk,
+                                              int ne, bool has_q, const uint8_t *stage, int h,
+                                              int lane) {
+  constexpr int kChunk = Tiling<T>::kResChunk;
+  const int e0 = chunk * kChunk;
   const T *row = static_cast<const T *>(p.logits) + static_cast<size_t>(d.slot) * p.V;
   const float *qrow =
-      inf.has_q ? p.q + (static_cast<size_t>(d.b) * p.gmax + d.k) * p.V : nullptr;
-  const float *sq = reinterpret_cast<const float *>(stage + K2Shape<T>::kLBytes);
+      has_q ? p.q + (static_cast<size_t>(d.b) * p.gmax + d.k) * p.V : nullptr;
+  const float *sq = reinterpret_cast<const float *>(stage + kChunk * sizeof(T));
   const float2 negm = make_float2(-d.m, -d.m), cs2 = make_float2(d.cs, d.cs);
   const float2 inv2 = make_float2(d.inv_s, d.inv_s), zero2 = make_float2(0.f, 0.f);
-  const bool onehot = d.tok >= 0 && !inf.has_q;
-  const int nsg = (inf.ne + kSeg - 1) / kSeg;
+  const bool onehot = d.tok >= 0 && !has_q;
+  const int nsg = (ne + kSeg - 1) / kSeg;
   float chunk_r = 0.f, chunk_p = 0.f;
-  for (int sgi = 0; sgi < nsg; ++sgi) {
+  for (int sgi = h; sgi < nsg; sgi += 2) {
     float2 ar = zero2, ap = zero2;
 #pragma unroll
     for (int step = 0; step < kSeg / 256; ++step) {
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int e = sgi * kSeg + step * 256 + half * 128 + 4 * lane;  // in chunk
-        if (e < inf.ne) {
+        if (e < ne) {
           float2 x01, x23, q01 = zero2, q23 = zero2;  // q held negated
           if (kTMA) {
             if constexpr (sizeof(T) == 2) {
@@ -347,7 +373,7 @@ __device__ __forceinline__ void chunk_resid(const Params &p, const ItemInfo2 &in
               x01 = make_float2(w.x, w.y);
               x23 = make_float2(w.z, w.w);
             }
-            if (inf.has_q) {
+            if (has_q) {
               const float4 w = *reinterpret_cast<const float4 *>(sq + e);
               q01 = make_float2(-w.x, -w.y);
               q23 = make_float2(-w.z, -w.w);
@@ -357,7 +383,7 @@ __device__ __forceinline__ void chunk_resid(const Params &p, const ItemInfo2 &in
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
               // elements past the chunk end weigh nothing (p = q = 0 there)
-              const bool in = e + t < inf.ne;
+              const bool in = e + t < ne;
               xs[t] = in ? Elem<T>::load(row, e0 + e + t) : -INFINITY;
               qs[t] = (in && qrow) ? -__ldg(qrow + e0 + e + t) : 0.f;
             }
@@ -387,120 +413,13 @@ __device__ __forceinline__ void chunk_resid(const Params &p, const ItemInfo2 &in
     const float sr = warp_sum(ar.x + ar.y);
     const float sp = warp_sum(ap.x + ap.y);
     if (lane == 0) {
-      p.ssum[static_cast<size_t>(d.b) * p.nseg + inf.c * K2Shape<T>::kSegPerChunk + sgi] =
+      p.ssum[static_cast<size_t>(sl) * p.nseg + chunk * Tiling<T>::kSegPerChunk + sgi] =
           make_float2(sr, sp);
       chunk_r += sr;
       chunk_p += sp;
     }
   }
-  if (lane == 0) p.csum[static_cast<size_t>(d.b) * p.C2 + inf.c] = make_float2(chunk_r, chunk_p);
-}
-
-// ------------------------------------------------------------- kernel ----
-
-template <typename T, bool kTMA>
-__global__ void __launch_bounds__(K2Shape<T>::kThreads, 1) sv_resample_kernel(Params p) {
-  using S = K2Shape<T>;
-  extern __shared__ __align__(128) uint8_t smem[];
-  const size_t stage_bytes = kTMA ? static_cast<size_t>(S::kStages) * S::kStageBytes : 0;
-  ItemInfo2 *info = reinterpret_cast<ItemInfo2 *>(smem + stage_bytes);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(info + S::kStages);
-  const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + S::kStages);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S::kStages; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-  pdl_wait();
-  uint32_t *err = &p.hdr->err;
-
-  if (warp == 0) {
-    if (lane != 0) return;
-    // ------------------------------------------------ producer lane ----
-    const uint64_t pol_l = policy_evict_normal(), pol_q = policy_evict_first();
-    // 32-bit item arithmetic (item counts are below B * C2 < 2^31): this lane
-    // issues every copy of the CTA and must stay cheap.
-    const int nq = static_cast<int>(ld_cg(&p.hdr->n_q)), nn = static_cast<int>(ld_cg(&p.hdr->n_noq));
-    const int C = p.C2, total = (nq + nn) * C;
-    uint32_t n = 0;
-    int cur = -1;
-    Desc d{};
-    bool ok = true;
-    // Item indices come from a global counter; the next one is requested
-    // while the current one is issued, hiding the atomic's latency.
-    int it = static_cast<int>(atomicAdd(&p.hdr->k2_next, 1u));
-    while (it < total) {
-      const int nxt = static_cast<int>(atomicAdd(&p.hdr->k2_next, 1u));
-      const int li = it / C;  // rows that read q come first in the item order
-      const int c = it - li * C;
-      const bool hq = li < nq;
-      if (li != cur) {
-        d = ld_cg(hq ? p.desc_q + li : p.desc_noq + (li - nq));
-        cur = li;
-      }
-      const int e0 = c * S::kChunk, ne = min(S::kChunk, p.V - e0);
-      const int s = static_cast<int>(n % S::kStages);
-      const uint32_t ph = (n / S::kStages) & 1u;
-      if (n >= S::kStages && !(ok = mbar_wait(empty0 + 8 * s, ph ^ 1u, err))) break;
-      info[s] = ItemInfo2{d, c, ne, hq ? 1 : 0, 0};
-      if (kTMA) {
-        const uint32_t lb = static_cast<uint32_t>(ne) * sizeof(T);
-        const uint32_t qb = hq ? static_cast<uint32_t>(ne) * 4u : 0u;
-        uint8_t *st = smem + static_cast<size_t>(s) * S::kStageBytes;
-        mbar_arrive_expect_tx(full0 + 8 * s, lb + qb);
-        tma_load_1d(smem_addr(st),
-                    static_cast<const T *>(p.logits) + static_cast<size_t>(d.slot) * p.V + e0,
-                    lb, full0 + 8 * s, pol_l);
-        if (hq)
-          tma_load_1d(smem_addr(st + S::kLBytes),
-                      p.q + (static_cast<size_t>(d.b) * p.gmax + d.k) * p.V + e0, qb,
-                      full0 + 8 * s, pol_q);
-      } else {
-        mbar_arrive(full0 + 8 * s);
-      }
-      ++n;
-      it = nxt;
-    }
-    for (int w = 0; ok && w < S::kConsumers; ++w, ++n) {
-      const int s = static_cast<int>(n % S::kStages);
-      const uint32_t ph = static_cast<uint32_t>((n / S::kStages) & 1);
-      if (n >= S::kStages && !(ok = mbar_wait(empty0 + 8 * s, ph ^ 1u, err))) break;
-      info[s].c = -1;
-      mbar_arrive(full0 + 8 * s);
-    }
-    for (uint32_t j = (n > S::kStages ? n - S::kStages : 0); j < n; ++j)
-      mbar_wait(full0 + 8 * static_cast<int>(j % S::kStages),
-                static_cast<uint32_t>((j / S::kStages) & 1), err);
-    return;
-  }
-
-  // ---------------------------------------------------- consumer warps ----
-  const int cw = warp - 1;
-  for (uint32_t n = cw;; n += S::kConsumers) {
-    const int s = static_cast<int>(n % S::kStages);
-    const uint32_t ph = static_cast<uint32_t>((n / S::kStages) & 1);
-    if (!mbar_wait(full0 + 8 * s, ph, err)) break;
-    const ItemInfo2 inf = info[s];
-    if (inf.c < 0) break;
-    chunk_resid<T, kTMA>(p, inf, smem + (kTMA ? static_cast<size_t>(s) * S::kStageBytes : 0),
-                         lane);
-    __syncwarp();
-    uint32_t old = 0;
-    if (lane == 0) {
-      mbar_arrive(empty0 + 8 * s);
-      old = atomic_add_acq_rel(&p.k2_cnt[inf.d.b], 1u);
-    }
-    old = __shfl_sync(kFull, old, 0);
-    if (old + 1 == static_cast<uint32_t>(p.C2)) {
-      __threadfence();
-      search_request<T, kTMA>(p, inf.d, lane);
-    }
-  }
+  return make_float2(chunk_r, chunk_p);
 }
 
 }  // namespace sv

@@ -1,0 +1,602 @@
+// sv_verify.cuh -- the persistent verification kernel.
+//
+// One CTA per SM runs the whole verification step of a batch (after the
+// small set-up kernel 0), on two kinds of work item:
+//
+//   row-statistics items  every (active row, vocabulary chunk) of the target
+//                         logits, handed out from a global counter in blocks,
+//                         request after request (tutorial page
+//                         dpshk.com/news/5598276, §5.2 steps (1)-(4));
+//   residual items        for each request that draws a token from a
+//                         distribution (T > 0), every chunk of the one row
+//                         it draws from (§3.1 step 4, §5.2 step (5), §5.3),
+//                         handed out from a second counter in the order the
+//                         requests' merges publish their rows.
+//
+// Because row blocks go out request after request, requests complete while
+// the stream runs, and the row a request draws from was read moments before:
+// its re-read is mostly served by L2.  No CTA ever waits for a specific other
+// CTA: all work is claimed dynamically, so progress does not depend on which
+// CTAs are resident.
+//
+// Roles inside a CTA:
+//   claimer lane    claims blocks of work (all the global round trips of
+//                   work distribution) and queues them for the producer;
+//   producer lane   streams each item of a claimed block into a shared-memory
+//                   stage with 1-D TMA bulk copies (logits, plus q for a
+//                   residual item) and observes item completions in issue
+//                   order through the stage-release barriers;
+//   consumer pairs  two warps reduce one item together, each half of it
+//                   (chunk statistics or residual sums), and combine;
+//   counter warp    adds completed runs of items to the requests' global
+//                   counters (a batch of runs at once, one per lane) and
+//                   appends a job to the global job queue for each run that
+//                   completed a request;
+//   job warp        takes tickets from the global job queue and runs the
+//                   job it draws: the merge + accept step of a request or
+//                   the inverse-CDF search of its residual.  Jobs go to
+//                   whichever CTA asks next, so they run in parallel across
+//                   the grid whatever CTA completed the requests.
+// Every wait is bounded (about 2 s of %globaltimer); a timeout sets
+// SV_FAULT_TIMEOUT and the CTA leaves in order.
+#pragma once
+
+#include "sv_device.cuh"
+#include "sv_layout.cuh"
+#include "sv_resample.cuh"
+#include "sv_rowstats.cuh"
+
+namespace sv {
+
+#ifndef SV_PAIRS
+#define SV_PAIRS 4
+#endif
+#ifndef SV_STAGES
+#define SV_STAGES 8
+#endif
+#ifndef SV_ROW_BLOCK
+#define SV_ROW_BLOCK 8
+#endif
+#ifndef SV_RES_BLOCK
+#define SV_RES_BLOCK 4
+#endif
+#ifndef SV_CLAIM_SLOTS
+#define SV_CLAIM_SLOTS 2
+#endif
+#ifndef SV_POLL_NS
+#define SV_POLL_NS 0
+#endif
+constexpr int kPairs = SV_PAIRS;             // consumer pairs
+constexpr int kStages = SV_STAGES;
+constexpr int kRowBlock = SV_ROW_BLOCK;      // row-statistics items per claim
+constexpr int kResBlock = SV_RES_BLOCK;      // residual items per claim
+constexpr int kClaimSlots = SV_CLAIM_SLOTS;  // claimed blocks queued ahead
+constexpr unsigned kPollNs = SV_POLL_NS;      // pause between polls of a global flag
+constexpr int kWarpProducer = 0, kWarpClaimer = 1, kWarpConsumer0 = 2;
+constexpr int kWarpCounter = kWarpConsumer0 + 2 * kPairs, kWarpJob = kWarpCounter + 1;
+constexpr int kThreads = 32 * (kWarpJob + 1);
+constexpr int kSmemReq = 2048;  // requests whose row offsets and scales sit in shared memory
+constexpr int kRunRing = 32;
+static_assert(kStages % kPairs == 0, "each consumer pair owns whole stages");
+static_assert(kRunRing > kStages + 1, "every open run fits (each holds an unobserved item)");
+
+struct Item {
+  int kind;   // 0 row statistics, 1 residual, -1 end of stream
+  int c;      // chunk within the row
+  int ne;     // elements in the chunk
+  int has_q;  // residual item reads a q chunk
+  int slot;   // row statistics: padded row index; residual: descriptor slot
+  float cs;   // row statistics: log2(e) / T (0: greedy)
+  int pad[2];
+  Desc d;     // residual item: the row and its statistics
+};
+
+// A block of work claimed by the claimer lane.
+struct Claim {
+  int kind;  // 0 row items [a, a_end), 1 residual chunks [c0, c1) of slot b, -1 end
+  uint32_t a, a_end;
+  int b, c0, c1;
+  int pad[2];
+  Desc d;    // residual: the slot's published row
+};
+
+// A run of consecutive items of one request (one kind) issued by a CTA.
+struct Run {
+  int kind;       // 0 row statistics, 1 residual
+  int id;         // request (row statistics) or descriptor slot (residual)
+  int count;
+  int nr;         // rows of the request (row statistics)
+  uint32_t last;  // local index of the run's last item
+};
+
+// A completed run, handed from the producer lane to the counter warp.
+struct Done {
+  int kind;  // 0, 1 as in Run; -1 end of stream
+  int id;
+  int count;
+  int nr;
+};
+
+
+constexpr size_t verify_smem_bytes() {
+  return static_cast<size_t>(kStages) * kStageBytes + kStages * sizeof(Item) +
+         2 * kStages * sizeof(uint64_t);
+}
+
+template <typename T, bool kTMA>
+__global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ SvcQueue<Done> svcq_s;
+  __shared__ SvcQueue<Claim, kClaimSlots> clq_s;
+  __shared__ float2 xch_s[kStages];     // half 1's partial result of the stage's item
+  __shared__ uint64_t xbar_s[kStages];  // ... and the barrier that hands it over
+  __shared__ int row_start_s[kSmemReq + 1];
+  __shared__ float cs_s[kSmemReq];
+  auto *svcq = &svcq_s;
+  auto *clq = &clq_s;
+  Item *info = reinterpret_cast<Item *>(smem + kStages * kStageBytes);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(info + kStages);
+  const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kStages);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int R = p.gmax + 1;
+  constexpr int kRowChunk = Tiling<T>::kRowChunk;
+  constexpr int kResChunk = Tiling<T>::kResChunk;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 2);  // both warps of the owning pair
+    }
+    for (int s = 0; s < kStages; ++s) mbar_init(smem_addr(&xbar_s[s]), 1);
+    svc_init(svcq);
+    svc_init(clq);
+    fence_mbar_init();
+  }
+  pdl_wait();  // kernel 0's row offsets, scales and reset counters
+  const bool smem_req = p.B <= kSmemReq;
+  if (smem_req) {
+    for (int i = threadIdx.x; i <= p.B; i += kThreads) row_start_s[i] = ld_cg(p.row_start + i);
+    for (int i = threadIdx.x; i < p.B; i += kThreads) cs_s[i] = ld_cg(p.cs + i);
+  }
+  __syncthreads();
+
+  const T *logits = static_cast<const T *>(p.logits);
+  uint32_t *err = &p.hdr->err;
+  auto row_start = [&](int b) { return smem_req ? row_start_s[b] : ld_cg(p.row_start + b); };
+  auto scale = [&](int b) { return smem_req ? cs_s[b] : ld_cg(p.cs + b); };
+
+  if (warp == kWarpCounter) {
+    // --------------------------------------------------- counter warp ----
+    // Takes entry k and whatever entries after it are already queued (lane j
+    // holds entry k + j), adds all their runs to the global counters at once
+    // and marks the job of every run that completed a request as due.
+    for (uint32_t k = 0;;) {
+      if (!mbar_wait_warp(smem_addr(&svcq->full[k % kSvcSlots]), (k / kSvcSlots) & 1u, err))
+        break;
+      const uint32_t kj = k + lane;
+      const bool queued = lane == 0 || mbar_test_wait(smem_addr(&svcq->full[kj % kSvcSlots]),
+                                                      (kj / kSvcSlots) & 1u);
+      const unsigned qm = __ballot_sync(kFull, queued);
+      const int nb = qm == kFull ? 32 : __ffs(~qm) - 1;
+      Done e{-2, 0, 0, 0};
+      if (lane < nb) e = svcq->slot[kj % kSvcSlots];
+      __syncwarp();
+      if (lane < nb) mbar_arrive(smem_addr(&svcq->empty[kj % kSvcSlots]));
+      k += nb;
+      bool last = false;
+      if (e.kind >= 0) {
+        __threadfence();  // the run's results (observed by the producer) go first
+        uint32_t *cnt = e.kind == 0 ? p.k1_cnt + e.id : p.k2_cnt + e.id;
+        const uint32_t total = e.kind == 0 ? static_cast<uint32_t>(e.nr * p.C1)
+                                           : static_cast<uint32_t>(p.C2);
+        last = atomicAdd(cnt, static_cast<uint32_t>(e.count)) + e.count == total;
+        if (last) fence_acq_rel();  // acquire every other run's results
+      }
+      // Job due: the merge of request id, or the search of slot id.  The
+      // fence above orders every run's results before this flag.
+      if (last) st_relaxed(p.jflag + (e.kind == 0 ? 0 : p.B) + e.id, kJobDue);
+      if (__any_sync(kFull, e.kind == -1)) break;
+    }
+    return;
+  }
+
+  if (warp == kWarpJob) {
+    // ------------------------------------------------------- job warp ----
+    // Tickets over the 2B job flags: job b < B merges request b, job B + s
+    // searches slot s.  A ticket waits until its job is due or will never
+    // be (a request without rows, a slot left unused, or -- once every
+    // request is merged -- a slot never reserved).
+    const uint32_t njobs = 2u * static_cast<uint32_t>(p.B);
+    for (;;) {
+      int state = 0;  // 1 due, 2 none (next ticket), 3 no more jobs or timeout
+      uint32_t h = 0;
+      if (lane == 0) {
+        h = atomicAdd(&p.hdr->jq_head, 1u);
+        if (h >= njobs) state = 3;
+        const uint64_t t0 = global_timer_ns();
+        while (state == 0) {
+          const uint32_t f = ld_acquire(p.jflag + h);
+          if (f == kJobDue) {
+            state = 1;
+          } else if (f == kJobNone) {
+            state = 2;
+          } else if (h >= static_cast<uint32_t>(p.B) && ld_acquire(&p.hdr->all_merged) != 0u &&
+                     h - p.B >= ld_relaxed(&p.hdr->b_reserved)) {
+            state = 3;
+          } else if (global_timer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(err, SV_FAULT_TIMEOUT);
+            state = 3;
+          } else if (kPollNs) {
+            __nanosleep(kPollNs);
+          }
+        }
+      }
+      __syncwarp();  // lane 0's acquire of the flag orders every lane's reads
+      state = __shfl_sync(kFull, state, 0);
+      if (state == 3) break;
+      if (state == 2) continue;
+      const int id = static_cast<int>(__shfl_sync(kFull, h, 0));
+      if (id < p.B) {
+        const int rows = row_start(id + 1) - row_start(id);
+        merge_request<T>(p, id, rows, scale(id), lane);
+      } else {
+        search_request<T, kTMA>(p, ld_cg(p.desc + (id - p.B)), id - p.B, lane);
+      }
+    }
+    return;
+  }
+
+  if (warp == kWarpClaimer) {
+    if (lane != 0) return;
+    // -------------------------------------------------- claimer lane ----
+    // Residual work is numbered by descriptor slot (merge order): chunk c of
+    // slot s is item s * C2 + c.  While this CTA can still claim rows, it
+    // takes residual work only from a slot already written, with one
+    // compare-and-swap per pass (a lost race falls through to row work, so
+    // it never waits).  Once rows are gone it takes tickets from the same
+    // counter (atomicAdd: no race to lose), possibly ahead of the slot's
+    // reservation, and waits for them; only CTAs without rows wait, so every
+    // row is claimed, every request merged and every ticket resolved.  A
+    // ticket past the last reserved slot, once every request is merged, ends
+    // the stream.  Row blocks are claimed one ahead, so the claim's round
+    // trip overlaps the queueing of the block before.
+    const uint32_t n_row_items = ld_cg(&p.hdr->n_rows) * static_cast<uint32_t>(p.C1);
+    const uint32_t C2 = static_cast<uint32_t>(p.C2);
+    // Claim sizes: up to kRowBlock / kResBlock items, fewer when the batch
+    // is small, so that its items spread over the grid.
+    const uint32_t spread = 2u * gridDim.x;
+    const uint32_t rb = min(static_cast<uint32_t>(kRowBlock), max(1u, n_row_items / spread));
+    const uint32_t rt = min(static_cast<uint32_t>(kResBlock),
+                            max(1u, ld_cg(&p.hdr->n_valid) * C2 / spread));
+    uint32_t k = 0;
+    bool ok = true;
+    auto push = [&](const Claim &c) { ok = ok && svc_push(clq, k++, c, err); };
+    // Slot s: kReadySample or kReadySkip once written; 0 when it will never
+    // be (every request merged, fewer slots reserved) or on a timeout.
+    auto await_slot = [&](uint32_t sl) -> uint32_t {
+      if (sl >= static_cast<uint32_t>(p.B)) return 0u;  // at most one slot per request
+      const uint64_t t0 = global_timer_ns();
+      for (;;) {
+        const uint32_t f = ld_acquire(p.ready + sl);
+        if (f != kPending) return f;
+        // All merged: every reservation is visible, b_reserved is final.
+        if (ld_acquire(&p.hdr->all_merged) != 0u && sl >= ld_relaxed(&p.hdr->b_reserved))
+          return 0u;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          atomicOr(err, SV_FAULT_TIMEOUT);
+          ok = false;
+          return 0u;
+        }
+        if (kPollNs) __nanosleep(kPollNs);
+      }
+    };
+    uint32_t a_cur = atomicAdd(&p.hdr->a_next, rb);
+    bool rows_left = true, more = true;
+    while (ok && more) {
+      if (rows_left) {
+        const uint2 bc = ld_relaxed2(&p.hdr->b_next);  // {b_next, b_reserved}
+        const uint32_t sl = bc.x / C2;
+        if (sl < bc.y) {
+          const uint32_t f = ld_acquire(p.ready + sl);
+          const uint32_t s_end = (sl + 1) * C2;
+          if (f == kReadySkip) {
+            atomicMax(&p.hdr->b_next, s_end);
+            continue;
+          }
+          if (f == kReadySample) {
+            const uint32_t want = min(bc.x + rt, s_end);
+            if (atomicCAS(&p.hdr->b_next, bc.x, want) == bc.x) {
+              const int c0 = static_cast<int>(bc.x - sl * C2);
+              push(Claim{1, 0u, 0u, static_cast<int>(sl), c0, c0 + static_cast<int>(want - bc.x),
+                         {0, 0}, ld_cg(p.desc + sl)});
+              continue;
+            }
+          }
+        }
+        if (a_cur < n_row_items) {
+          const uint32_t a_pre = atomicAdd(&p.hdr->a_next, rb);
+          push(Claim{0, a_cur, min(a_cur + rb, n_row_items), 0,
+                     0, 0, {0, 0}, Desc{}});
+          a_cur = a_pre;
+          continue;
+        }
+        rows_left = false;
+      }
+      // A ticket: residual items [r, r + rt), slot by slot.
+      const uint32_t r = atomicAdd(&p.hdr->b_next, rt);
+      for (uint32_t it = r, r_end = r + rt; ok && it < r_end;) {
+        const uint32_t sl = it / C2, s_end = (sl + 1) * C2;
+        const uint32_t f = await_slot(sl);
+        if (f == 0u) {
+          more = false;
+          break;
+        }
+        const uint32_t seg_end = min(r_end, s_end);
+        if (f == kReadySample) {
+          const int c0 = static_cast<int>(it - sl * C2);
+          push(Claim{1, 0u, 0u, static_cast<int>(sl), c0, c0 + static_cast<int>(seg_end - it),
+                     {0, 0}, ld_cg(p.desc + sl)});
+        } else {
+          atomicMax(&p.hdr->b_next, s_end);  // an unused slot: pass it over
+        }
+        it = seg_end;
+      }
+    }
+    if (ok) push(Claim{-1, 0u, 0u, 0, 0, 0, {0, 0}, Desc{}});
+    return;
+  }
+
+  if (warp == kWarpProducer) {
+    if (lane != 0) return;
+    // -------------------------------------------------- producer lane ----
+    const uint64_t pol_l = policy_evict_normal(), pol_q = policy_evict_first();
+    uint32_t n = 0, m = 0, pushed = 0;  // items issued / observed released; runs handed over
+    bool ok = true;
+
+    // Open runs, oldest first (head in registers, the rest in a ring).
+    Run head{0, 0, 0, 0, 0u};
+    bool has_head = false;
+    Run ring[kRunRing];
+    int rh = 0, rc = 0;
+    auto add_run = [&](const Run &r) {
+      if (!has_head) {
+        head = r;
+        has_head = true;
+      } else {
+        ring[(rh + rc) % kRunRing] = r;
+        ++rc;
+      }
+    };
+    // Item m was released: hand its run over if it was the run's last item.
+    auto released = [&]() {
+      if (has_head && head.last == m) {
+        ok = svc_push(svcq, pushed++, Done{head.kind, head.id, head.count, head.nr}, err);
+        if (rc > 0) {
+          head = ring[rh];
+          rh = (rh + 1) % kRunRing;
+          --rc;
+        } else {
+          has_head = false;
+        }
+      }
+      ++m;
+    };
+    auto observe_through = [&](uint32_t j) {  // block until items <= j are released
+      while (ok && m <= j) {
+        ok = mbar_wait(empty0 + 8 * (m % kStages), (m / kStages) & 1u, err);
+        if (ok) released();
+      }
+    };
+    auto observe_ready = [&]() {  // take whatever releases have happened
+      bool any = false;
+      while (ok && m < n && mbar_test_wait(empty0 + 8 * (m % kStages), (m / kStages) & 1u)) {
+        released();
+        any = true;
+      }
+      return any;
+    };
+    auto next_stage = [&]() -> int {  // the stage item n uses, once it is free
+      if (n >= kStages) observe_through(n - kStages);
+      return static_cast<int>(n % kStages);
+    };
+    auto request_of_row = [&](int fr) {  // last request whose first row is <= fr
+      int lo = 0, hi = p.B;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (row_start(mid) <= fr) lo = mid;
+        else hi = mid;
+      }
+      return lo;
+    };
+
+    // Row-statistics items [a, a_end): flat row fr = a / C1, chunk a % C1.
+    auto issue_rows = [&](uint32_t a, uint32_t a_end) {
+      int fr = static_cast<int>(a / p.C1), c = static_cast<int>(a - fr * p.C1);
+      int b = request_of_row(fr), rs = row_start(b), re = row_start(b + 1);
+      while (fr >= re) {  // requests without rows share the offset
+        rs = re;
+        re = row_start(++b + 1);
+      }
+      float cs = scale(b);
+      bool fresh = true;
+      for (uint32_t it = a; ok && it < a_end; ++it, ++c) {
+        if (c == p.C1) {
+          c = 0;
+          if (++fr >= re) {
+            do {
+              rs = re;
+              re = row_start(++b + 1);
+            } while (fr >= re);
+            cs = scale(b);
+            fresh = true;
+          }
+        }
+        if (fresh) {
+          const int run = static_cast<int>(min(a_end, static_cast<uint32_t>(re) * p.C1) - it);
+          add_run(Run{0, b, run, re - rs, n + run - 1});
+          fresh = false;
+        }
+        const int s = next_stage();
+        if (!ok) return;
+        const int slot = b * R + (fr - rs);
+        const int e0 = c * kRowChunk, ne = min(kRowChunk, p.V - e0);
+        Item &inf = info[s];
+        inf.kind = 0;
+        inf.c = c;
+        inf.ne = ne;
+        inf.slot = slot;
+        inf.cs = cs;
+        if (kTMA) {
+          const uint32_t bytes = static_cast<uint32_t>(ne) * sizeof(T);
+          mbar_arrive_expect_tx(full0 + 8 * s, bytes);
+          tma_load_1d(smem_addr(smem + static_cast<size_t>(s) * kStageBytes),
+                      logits + static_cast<size_t>(slot) * p.V + e0, bytes, full0 + 8 * s,
+                      pol_l);
+        } else {
+          mbar_arrive(full0 + 8 * s);
+        }
+        ++n;
+      }
+    };
+
+    // Residual chunks [c0, c1) of descriptor slot sl, whose row is d.
+    auto issue_residual = [&](int sl, int c0, int c1, const Desc &d) {
+      add_run(Run{1, sl, c1 - c0, 0, n + static_cast<uint32_t>(c1 - c0) - 1});
+      const bool hq = d.tok >= 0 && p.q != nullptr;
+      for (int c = c0; ok && c < c1; ++c) {
+        const int s = next_stage();
+        if (!ok) return;
+        const int e0 = c * kResChunk, ne = min(kResChunk, p.V - e0);
+        Item &inf = info[s];
+        inf.kind = 1;
+        inf.c = c;
+        inf.ne = ne;
+        inf.has_q = hq ? 1 : 0;
+        inf.slot = sl;
+        inf.d = d;
+        if (kTMA) {
+          const uint32_t lb = static_cast<uint32_t>(ne) * sizeof(T);
+          const uint32_t qb = hq ? static_cast<uint32_t>(ne) * 4u : 0u;
+          uint8_t *st = smem + static_cast<size_t>(s) * kStageBytes;
+          mbar_arrive_expect_tx(full0 + 8 * s, lb + qb);
+          tma_load_1d(smem_addr(st), logits + static_cast<size_t>(d.slot) * p.V + e0, lb,
+                      full0 + 8 * s, pol_l);
+          if (hq)
+            tma_load_1d(smem_addr(st + kResChunk * sizeof(T)),
+                        p.q + (static_cast<size_t>(d.b) * p.gmax + d.k) * p.V + e0, qb,
+                        full0 + 8 * s, pol_q);
+        } else {
+          mbar_arrive(full0 + 8 * s);
+        }
+        ++n;
+      }
+    };
+
+    // Stream the claimed blocks; while none is queued, keep handing this
+    // CTA's completed runs to the counter warp (other CTAs' tickets may be
+    // waiting for the merges they complete).
+    for (uint32_t k = 0; ok; ++k) {
+      const int i = static_cast<int>(k % kClaimSlots);
+      const uint32_t fb = smem_addr(&clq->full[i]), fp = (k / kClaimSlots) & 1u;
+      const uint64_t t0 = global_timer_ns();
+      while (ok && !mbar_test_wait(fb, fp)) {
+        if (!observe_ready()) __nanosleep(64);
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          atomicOr(err, SV_FAULT_TIMEOUT);
+          ok = false;
+        }
+      }
+      if (!ok) break;
+      const Claim cl = clq->slot[i];
+      mbar_arrive(smem_addr(&clq->empty[i]));
+      if (cl.kind < 0) break;
+      if (cl.kind == 0) issue_rows(cl.a, cl.a_end);
+      else issue_residual(cl.b, cl.c0, cl.c1, cl.d);
+    }
+    // Hand over the last runs, then stop the counter warp and the consumers.
+    if (n > 0) observe_through(n - 1);
+    svc_push(svcq, pushed, Done{-1, 0, 0, 0}, err);
+    for (int w = 0; w < kPairs; ++w, ++n) {
+      const int s = static_cast<int>(n % kStages);
+      if (!ok && n >= kStages && !mbar_wait(empty0 + 8 * s, ((n / kStages) & 1u) ^ 1u, err))
+        break;
+      info[s].kind = -1;
+      mbar_arrive(full0 + 8 * s);
+    }
+    return;
+  }
+
+  // ---------------------------------------------------- consumer pairs ----
+  // Pair g takes items g, g + kPairs, ...; warp h of the pair reduces half
+  // h of each item and half 1 hands its partial to half 0, which writes the
+  // item's result.  Both warps release the stage.  The hand-over slot and
+  // its barrier belong to the stage: half 1 writes the slot again only once
+  // the stage is refilled, which needs half 0's release (after its read).
+  const int cw = warp - kWarpConsumer0, g = cw >> 1, h = cw & 1;
+  for (uint32_t n = g;; n += kPairs) {
+    const int s = static_cast<int>(n % kStages);
+    if (!mbar_wait_warp(full0 + 8 * s, (n / kStages) & 1u, err)) break;
+    const Item &inf = info[s];
+    const int kind = inf.kind;
+    if (kind < 0) break;
+    const uint8_t *stage = smem + static_cast<size_t>(s) * kStageBytes;
+    const uint32_t xbar = smem_addr(&xbar_s[s]), xpar = (n / kStages) & 1u;
+    bool ok = true;
+    if (kind == 0) {
+      const int c = inf.c, ne = inf.ne, slot = inf.slot;
+      const float cs = inf.cs;
+      const int ne0 = half0_len(ne);
+      const int off = h ? ne0 : 0, len = h ? ne - ne0 : ne0;
+      ChunkStat st;
+      if (kTMA) {
+        st = chunk_stats_smem(reinterpret_cast<const T *>(stage) + off, len, cs, lane);
+      } else {
+        st = chunk_stats_global<T>(logits + static_cast<size_t>(slot) * p.V, c * kRowChunk + off,
+                                   len, cs, lane);
+      }
+      if (cs == 0.f && __float_as_int(st.v) != 0x7fffffff)
+        st.v = __int_as_float(__float_as_int(st.v) + off);
+      if (h == 1) {
+        __syncwarp();
+        if (lane == 0) {
+          xch_s[s] = make_float2(st.m, st.v);
+          mbar_arrive(xbar);  // release: the partial
+        }
+      } else {
+        ok = mbar_wait_warp(xbar, xpar, err);
+        if (ok) {
+          const float2 o = xch_s[s];
+          st = combine_halves(st, ChunkStat{o.x, o.y}, cs);
+          if (cs == 0.f && __float_as_int(st.v) != 0x7fffffff)
+            st.v = __int_as_float(__float_as_int(st.v) + c * kRowChunk);
+          if (lane == 0) p.part1[static_cast<size_t>(slot) * p.C1 + c] = Part{st.m, st.v};
+        }
+      }
+    } else {
+      const Desc d = inf.d;
+      const int c = inf.c;
+      const int sl = inf.slot;
+      const float2 part =
+          chunk_resid<T, kTMA>(p, d, sl, c, inf.ne, inf.has_q != 0, stage, h, lane);
+      if (h == 1) {
+        __syncwarp();
+        if (lane == 0) {
+          xch_s[s] = part;
+          mbar_arrive(xbar);
+        }
+      } else {
+        ok = mbar_wait_warp(xbar, xpar, err);
+        if (ok && lane == 0) {
+          const float2 o = xch_s[s];
+          p.csum[static_cast<size_t>(sl) * p.C2 + c] =
+              make_float2(__fadd_rn(part.x, o.x), __fadd_rn(part.y, o.y));
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);  // release: publishes the item's results
+    if (!ok) break;
+  }
+}
+
+}  // namespace sv

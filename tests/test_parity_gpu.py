@@ -147,6 +147,31 @@ def test_invalid_inputs_are_isolated():
     assert word == 1 | 2 | 4 | 8 | 16 | 32
 
 
+def test_no_request_with_rows_ends_cleanly():
+    """Every draft length out of range: nothing is streamed or merged; the
+    call still ends without a timeout and marks every request."""
+    B, g, V = 6, 3, 5000
+    w = Workload("allbad", B, g, V, "bf16", 1.0, (0.5, 1.0), (0.0, 1.0), seed=15)
+    case = make_case(w, device=DEV)
+    case["draft_lens"] = torch.tensor([-1, g + 1, g + 5, -3, g + 1, -1], dtype=torch.int32,
+                                      device=DEV)
+    gpu = run_gpu(case)
+    ora = run_oracle(case)
+    compare(case, gpu, ora)
+    assert (gpu["num_accepted"] == -1).all()
+    rc, word = api.last_error(api.get_workspace(B, g, V, DEV))
+    assert rc == api.SV_ERR_BAD_INPUT_DATA and word == 1
+
+
+def test_all_greedy_batch_has_no_residual_work():
+    """T = 0 everywhere: requests merge but publish nothing to re-sample."""
+    w = Workload("greedy", 24, 4, 70000, "bf16", 2.0, (0.5, 1.0), (0.0,), seed=16)
+    rep, gpu, ora = check(make_case(w, device=DEV))
+    assert rep["bad"] == 0
+    rc, word = api.last_error(api.get_workspace(24, 4, 70000, DEV))
+    assert (rc, word) == (api.SV_OK, 0)
+
+
 def test_clean_call_reports_ok():
     case = make_case(workloads.workload("c1"), device=DEV)
     run_gpu(case)
