@@ -73,12 +73,27 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // SV_FAULT_TIMEOUT in the error word and returns false.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// try_wait that lets the thread sleep in hardware until the phase completes
+// (or about hint_ns pass), so waiting warps leave the issue slots and the
+// memory pipeline to the warps that work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; "
+      "selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
                                             uint32_t *err) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1; it < (1u << 30); ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) break;
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) break;
   }
   atomicOr(err, SV_FAULT_TIMEOUT);
   return false;

@@ -239,7 +239,7 @@ __device__ __forceinline__ int cdf_block8(int n, const float (&w)[8], float targ
 // segment sum, a walk over them finds the segment, a second wave fetches its
 // elements.  Longer rows walk chunk sums, segment sums, then elements.
 template <typename T, bool kVec>
-__device__ void search_request(const Params &p, const Desc &d, int sl, int lane) {
+__device__ __noinline__ void search_request(const Params &p, const Desc &d, int sl, int lane) {
   const float2 *cs2 = p.csum + static_cast<size_t>(sl) * p.C2;
   const float2 *ss2 = p.ssum + static_cast<size_t>(sl) * p.nseg;
   const int nsr = (p.V + kSeg - 1) / kSeg;  // segments of the row

@@ -204,7 +204,7 @@ constexpr int kMergeBatch = 16;
 // draft ids and uniforms, the first kMergeBatch chunk statistics of each
 // row), then the two gathers that need the draft id (l_x and q(x)).
 template <typename T>
-__device__ void merge_request(const Params &p, int b, int nr, float cs, int lane) {
+__device__ __noinline__ void merge_request(const Params &p, int b, int nr, float cs, int lane) {
   const int g = nr - 1;
   const int R = p.gmax + 1;
   const bool greedy = (cs == 0.f);

@@ -214,15 +214,17 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
         h = atomicAdd(&p.hdr->jq_head, 1u);
         if (h >= njobs) state = 3;
         const uint64_t t0 = global_timer_ns();
+        // Relaxed polls; one acquire fence once a flag is seen.
         while (state == 0) {
-          const uint32_t f = ld_acquire(p.jflag + h);
+          const uint32_t f = ld_relaxed(p.jflag + h);
           if (f == kJobDue) {
+            fence_acq_rel();
             state = 1;
           } else if (f == kJobNone) {
             state = 2;
-          } else if (h >= static_cast<uint32_t>(p.B) && ld_acquire(&p.hdr->all_merged) != 0u &&
-                     h - p.B >= ld_relaxed(&p.hdr->b_reserved)) {
-            state = 3;
+          } else if (h >= static_cast<uint32_t>(p.B) && ld_relaxed(&p.hdr->all_merged) != 0u) {
+            fence_acq_rel();  // b_reserved is final now
+            if (h - p.B >= ld_relaxed(&p.hdr->b_reserved)) state = 3;
           } else if (global_timer_ns() - t0 > kWaitLimitNs) {
             atomicOr(err, SV_FAULT_TIMEOUT);
             state = 3;
@@ -276,12 +278,17 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
     auto await_slot = [&](uint32_t sl) -> uint32_t {
       if (sl >= static_cast<uint32_t>(p.B)) return 0u;  // at most one slot per request
       const uint64_t t0 = global_timer_ns();
-      for (;;) {
-        const uint32_t f = ld_acquire(p.ready + sl);
-        if (f != kPending) return f;
+      for (;;) {  // relaxed polls; one acquire fence once a flag is seen
+        const uint32_t f = ld_relaxed(p.ready + sl);
+        if (f != kPending) {
+          fence_acq_rel();
+          return f;
+        }
         // All merged: every reservation is visible, b_reserved is final.
-        if (ld_acquire(&p.hdr->all_merged) != 0u && sl >= ld_relaxed(&p.hdr->b_reserved))
-          return 0u;
+        if (ld_relaxed(&p.hdr->all_merged) != 0u) {
+          fence_acq_rel();
+          if (sl >= ld_relaxed(&p.hdr->b_reserved)) return 0u;
+        }
         if (global_timer_ns() - t0 > kWaitLimitNs) {
           atomicOr(err, SV_FAULT_TIMEOUT);
           ok = false;
@@ -297,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
         const uint2 bc = ld_relaxed2(&p.hdr->b_next);  // {b_next, b_reserved}
         const uint32_t sl = bc.x / C2;
         if (sl < bc.y) {
-          const uint32_t f = ld_acquire(p.ready + sl);
+          const uint32_t f = ld_relaxed(p.ready + sl);
           const uint32_t s_end = (sl + 1) * C2;
           if (f == kReadySkip) {
             atomicMax(&p.hdr->b_next, s_end);
@@ -306,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
           if (f == kReadySample) {
             const uint32_t want = min(bc.x + rt, s_end);
             if (atomicCAS(&p.hdr->b_next, bc.x, want) == bc.x) {
+              fence_acq_rel();  // the slot's flag was seen: its descriptor is written
               const int c0 = static_cast<int>(bc.x - sl * C2);
               push(Claim{1, 0u, 0u, static_cast<int>(sl), c0, c0 + static_cast<int>(want - bc.x),
                          {0, 0}, ld_cg(p.desc + sl)});
