@@ -142,6 +142,15 @@ typedef struct {
                                              only; -1 for T > 0 rows)        */
     float *resid_mass;   /* [B] S = sum_j (p_k - q_k)_+ of the draw (NaN for
                                 greedy requests)                             */
+    int32_t *accept_hist;/* [gamma_max + 2] acceptance statistics of the
+                            batch in the same pass (P3 §6.2 logs the
+                            acceptance rate; §3.3 gives its expectation):
+                            accept_hist[j] = requests with num_accepted == j
+                            (j <= gamma_max), accept_hist[gamma_max + 1] =
+                            requests with invalid data.  Position i was
+                            accepted by sum_{j > i} accept_hist[j] requests.
+                            Zeroed by the call; no extra pass over the
+                            logits.                                          */
 } sv_diag;
 
 /* spec_verify plus the diagnostic outputs in `diag` (may be NULL). */

@@ -47,7 +47,7 @@ class SvDiag(ctypes.Structure):
     """Mirror of ``sv_diag``: device pointers, any may be NULL."""
     _fields_ = [("p_tok", _P), ("q_tok", _P), ("accept_prob", _P),
                 ("flags", _P), ("row_max", _P), ("row_sum", _P),
-                ("row_argmax", _P), ("resid_mass", _P)]
+                ("row_argmax", _P), ("resid_mass", _P), ("accept_hist", _P)]
 
 
 class SpecVerifyError(RuntimeError):
@@ -196,7 +196,8 @@ def verify(target_logits: torch.Tensor, draft_token_ids: torch.Tensor,
              "flags": torch.empty(B, g, dtype=torch.uint8, device=dev),
              "row_max": torch.empty(B, R, **f32), "row_sum": torch.empty(B, R, **f32),
              "row_argmax": torch.empty(B, R, dtype=torch.int32, device=dev),
-             "resid_mass": torch.empty(B, **f32)}
+             "resid_mass": torch.empty(B, **f32),
+             "accept_hist": torch.empty(g + 2, dtype=torch.int32, device=dev)}
         sd = SvDiag(**{k: v.data_ptr() for k, v in d.items()})
         rc = lib.spec_verify_diag(*args, ctypes.byref(sd))
     else:
@@ -206,6 +207,32 @@ def verify(target_logits: torch.Tensor, draft_token_ids: torch.Tensor,
     if diag:
         return out_tokens, out_num_accepted, d
     return out_tokens, out_num_accepted
+
+
+def acceptance_stats(accept_hist) -> dict:
+    """Acceptance statistics of one batch from ``accept_hist`` (the
+    ``sv_diag`` histogram, [gamma_max + 2]: requests per number of accepted
+    drafts, then requests with invalid data).  Host arithmetic only.
+
+    Returns n_valid, n_bad, accepted_at[i] (requests whose draft i was
+    accepted), reached[i] (requests that tested draft i and every earlier one
+    was accepted -- with uniform draft lengths, the requests whose draft i
+    was tested), the conditional acceptance rate accepted_at / reached per
+    position, and the mean number of emitted tokens (num_accepted + 1,
+    P3 §3.3)."""
+    h = [int(v) for v in (accept_hist.tolist() if hasattr(accept_hist, "tolist") else accept_hist)]
+    g = len(h) - 2
+    if g < 0:
+        raise ValueError("accept_hist must have gamma_max + 2 entries")
+    counts, n_bad = h[:g + 1], h[g + 1]
+    n_valid = sum(counts)
+    accepted_at = [sum(counts[j] for j in range(i + 1, g + 1)) for i in range(g)]
+    reached = [sum(counts[j] for j in range(i, g + 1)) for i in range(g)]
+    rate = [a / r if r else float("nan") for a, r in zip(accepted_at, reached)]
+    mean_emitted = (sum((j + 1) * c for j, c in enumerate(counts)) / n_valid
+                    if n_valid else float("nan"))
+    return {"n_valid": n_valid, "n_bad": n_bad, "accepted_at": accepted_at,
+            "reached": reached, "rate": rate, "mean_emitted": mean_emitted}
 
 
 def verify_host(target_logits: torch.Tensor, draft_token_ids: torch.Tensor,

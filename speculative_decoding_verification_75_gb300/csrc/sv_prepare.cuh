@@ -46,6 +46,8 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prepare_kernel(Params p) {
   __shared__ int carry, valid;
   __shared__ uint32_t err_acc;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (p.diag.accept_hist)
+    for (int j = tid; j < p.gmax + 2; j += kPrepThreads) p.diag.accept_hist[j] = 0;
   if (tid == 0) {
     carry = 0;
     valid = 0;
@@ -67,6 +69,7 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prepare_kernel(Params p) {
       if (nr == 0) {
         fill_bad_request(p, b);
         atomicOr(&err_acc, SV_BAD_DRAFT_LEN);
+        if (p.diag.accept_hist) atomicAdd(p.diag.accept_hist + p.gmax + 1, 1);
       } else {
         atomicAdd(&valid, 1);
       }

@@ -357,6 +357,7 @@ __device__ __noinline__ void merge_request(const Params &p, int b, int nr, float
         p.jflag[p.B + pos] = kJobNone;
         st_release(&p.ready[pos], kReadySkip);
       }
+      if (dg.accept_hist) atomicAdd(dg.accept_hist + p.gmax + 1, 1);
       count_merged(p);
     }
     return;
@@ -391,6 +392,7 @@ __device__ __noinline__ void merge_request(const Params &p, int b, int nr, float
   }
   if (lane == 0) {
     p.out_nacc[b] = k;
+    if (dg.accept_hist) atomicAdd(dg.accept_hist + k, 1);
     count_merged(p);
   }
 }

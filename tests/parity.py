@@ -112,6 +112,16 @@ def compare(case, gpu, ora, *, allow_borderline=True):
     a, o = gpu["resid_mass"][sm].astype(np.float64), ora["resid_mass"][sm]
     assert (np.abs(a - o) <= RESID_ATOL + REL * np.abs(o)).all(), "residual mass differs"
 
+    # Acceptance histogram (same pass): the GPU's own num_accepted exactly,
+    # and the oracle's except for the borderline requests.
+    if "accept_hist" in gpu:
+        hist = gpu["accept_hist"].astype(np.int64)
+        own = np.bincount(gpu["num_accepted"][~bad], minlength=g + 1)[:g + 1]
+        assert np.array_equal(hist[:g + 1], own), "accept_hist differs from num_accepted"
+        assert hist[g + 1] == int(bad.sum()), "accept_hist bad-request count differs"
+        ref = np.bincount(ora["num_accepted"][~bad], minlength=g + 1)[:g + 1]
+        assert np.abs(hist[:g + 1] - ref).sum() <= 2 * int(border.sum()), "accept_hist vs oracle"
+
     # Inside the band a decision may differ by rounding, but fp32 rounding is
     # far below the band: most borderline requests must still match exactly,
     # so a systematic error cannot hide behind the band.
