@@ -166,6 +166,45 @@ SV_API sv_status spec_verify_diag(const void *target_logits, sv_dtype logits_dty
                            const sv_diag *diag);
 
 /*
+ * KV rollback hand-off after verification (P3 §5.4: the KV of the drafted
+ * tokens is written first and marked tentative; after verification the cache
+ * is cut at num_accepted and the blocks past the cut go back to the block
+ * pool; the corrected token's KV is computed by the next step).
+ *
+ * For a paged KV cache, per request b with L = seq_lens[b] committed tokens
+ * before the drafts, g = draft_lens[b] (NULL: gamma_max) drafts at positions
+ * L .. L+g-1, and k = num_accepted[b] kept (as returned by spec_verify;
+ * k < 0, an invalid request, keeps none):
+ *   the entries j in [ceil((L+k)/block_size), ceil((L+g)/block_size)) of
+ *   block_tables[b] that hold a block id (>= 0) are appended to free_list at
+ *   free_list[*free_count ...] (in no particular order) and set to -1, and
+ *   seq_lens[b] becomes L + k.
+ * Device pointers: num_accepted, draft_lens [B]; seq_lens [B] (in/out);
+ * block_tables [B, max_blocks] (in/out); free_list [free_capacity];
+ * free_count a device int32 (in/out); status an optional device uint32 that
+ * receives SV_KV_* bits (OR-ed; the caller zeroes it).  Asynchronous on
+ * `stream`; allocates nothing.
+ * Problems in the data never fault: a request with an invalid draft length
+ * or a negative length is left unchanged (SV_KV_BAD_LENGTH); entries past
+ * max_blocks are not touched (SV_KV_TABLE_SHORT); an entry that should hold
+ * a block but is -1 is skipped (SV_KV_MISSING_BLOCK); a block that does not
+ * fit in the free list stays in the table, *free_count stops at
+ * free_capacity (SV_KV_FREE_LIST_FULL) and seq_lens is still updated.
+ * Returns SV_ERR_INVALID_ARG for negative sizes, block_size < 1, NULL
+ * required pointers or B * max_blocks beyond int32 indexing; SV_OK for
+ * B == 0 (nothing launched).
+ */
+#define SV_KV_FREE_LIST_FULL 0x1u
+#define SV_KV_MISSING_BLOCK 0x2u
+#define SV_KV_BAD_LENGTH 0x4u
+#define SV_KV_TABLE_SHORT 0x8u
+SV_API sv_status sv_kv_rollback(const int32_t *num_accepted, const int32_t *draft_lens,
+                                int32_t *seq_lens, int32_t *block_tables, int B,
+                                int gamma_max, int max_blocks, int block_size,
+                                int32_t *free_list, int32_t *free_count,
+                                int free_capacity, uint32_t *status, sv_stream_t stream);
+
+/*
  * Reads the error word of the last call that used `workspace` (synchronises
  * `stream`).  *out_word (may be NULL) receives the SV_BAD_* / SV_FAULT_*
  * bits.  Returns SV_ERR_TIMEOUT if a bounded wait gave up, else

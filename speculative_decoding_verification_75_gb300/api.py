@@ -37,7 +37,13 @@ SV_FAULT_TIMEOUT = 0x10000
 
 # Every symbol include/spec_verify.h declares.
 EXPORTS = ("sv_workspace_bytes", "spec_verify", "spec_verify_diag",
-           "sv_last_error", "sv_status_string", "spec_verify_noalloc")
+           "sv_last_error", "sv_status_string", "spec_verify_noalloc", "sv_kv_rollback")
+
+# Bits of the status word of sv_kv_rollback (include/spec_verify.h).
+SV_KV_FREE_LIST_FULL = 0x1
+SV_KV_MISSING_BLOCK = 0x2
+SV_KV_BAD_LENGTH = 0x4
+SV_KV_TABLE_SHORT = 0x8
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -86,6 +92,8 @@ def load_library():
     lib.sv_last_error.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint32)]
     lib.sv_status_string.restype = ctypes.c_char_p
     lib.sv_status_string.argtypes = [_I]
+    lib.sv_kv_rollback.restype = _I
+    lib.sv_kv_rollback.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P]
     _lib = lib
     return lib
 
@@ -207,6 +215,46 @@ def verify(target_logits: torch.Tensor, draft_token_ids: torch.Tensor,
     if diag:
         return out_tokens, out_num_accepted, d
     return out_tokens, out_num_accepted
+
+
+def kv_rollback(num_accepted: torch.Tensor, seq_lens: torch.Tensor,
+                block_tables: torch.Tensor, block_size: int, free_list: torch.Tensor,
+                free_count: torch.Tensor, draft_lens: Optional[torch.Tensor] = None, *,
+                gamma_max: Optional[int] = None, status: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> None:
+    """KV rollback after verification, in place, through ``sv_kv_rollback``.
+
+    num_accepted [B] int32 (from ``verify``), seq_lens [B] int32 (committed
+    tokens before the drafts; updated to L + k), block_tables [B, max_blocks]
+    int32 (-1 = no block; freed entries become -1), free_list [capacity]
+    int32 and free_count [1] int32 (freed block ids are appended), draft_lens
+    [B] int32 or None (then gamma_max drafts each), status [1] int32/uint32
+    or None (receives SV_KV_* bits; the caller zeroes it).  All CUDA tensors
+    on one device; asynchronous on the current (or given) stream."""
+    lib = load_library()
+    B = seq_lens.shape[0] if seq_lens.dim() == 1 else -1
+    if B < 0 or block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("seq_lens must be [B] and block_tables [B, max_blocks]")
+    dev = seq_lens.device
+    if gamma_max is None:
+        if draft_lens is None:
+            raise ValueError("gamma_max is needed when draft_lens is None")
+        gamma_max = int(draft_lens.max().item()) if B else 0
+    _check(num_accepted, "num_accepted", torch.int32, (B,), dev)
+    _check(seq_lens, "seq_lens", torch.int32, (B,), dev)
+    _check(block_tables, "block_tables", torch.int32, tuple(block_tables.shape), dev)
+    _check(draft_lens, "draft_lens", torch.int32, (B,), dev)
+    _check(free_list, "free_list", torch.int32, (free_list.numel(),), dev)
+    _check(free_count, "free_count", torch.int32, (1,), dev)
+    if status is not None and (status.device != dev or status.numel() != 1
+                               or status.dtype not in (torch.int32, torch.uint32)):
+        raise ValueError("status must be a 1-element int32/uint32 tensor on the same device")
+    rc = lib.sv_kv_rollback(_ptr(num_accepted), _ptr(draft_lens), _ptr(seq_lens),
+                            _ptr(block_tables), B, int(gamma_max), block_tables.shape[1],
+                            int(block_size), _ptr(free_list), _ptr(free_count),
+                            free_list.numel(), _ptr(status), _stream_handle(stream, dev))
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, lib)
 
 
 def acceptance_stats(accept_hist) -> dict:

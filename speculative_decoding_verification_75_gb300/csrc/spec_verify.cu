@@ -21,6 +21,7 @@
 #include "spec_verify.h"
 #include "sv_device.cuh"
 #include "sv_layout.cuh"
+#include "sv_kv.cuh"
 #include "sv_prepare.cuh"
 #include "sv_verify.cuh"
 
@@ -194,6 +195,27 @@ sv_status sv_last_error(const void *workspace, sv_stream_t stream, uint32_t *out
   if (word & SV_FAULT_TIMEOUT) return SV_ERR_TIMEOUT;
   if (word) return SV_ERR_BAD_INPUT_DATA;
   return SV_OK;
+}
+
+sv_status sv_kv_rollback(const int32_t *num_accepted, const int32_t *draft_lens,
+                         int32_t *seq_lens, int32_t *block_tables, int B, int gamma_max,
+                         int max_blocks, int block_size, int32_t *free_list,
+                         int32_t *free_count, int free_capacity, uint32_t *status,
+                         sv_stream_t stream) {
+  if (B < 0 || gamma_max < 0 || max_blocks < 0 || block_size < 1 || free_capacity < 0)
+    return SV_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * max_blocks >= INT_MAX ||
+      static_cast<long long>(max_blocks) * block_size >= INT_MAX)
+    return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!num_accepted || !seq_lens || !block_tables || !free_count ||
+      (free_capacity > 0 && !free_list))
+    return SV_ERR_INVALID_ARG;
+  sv::KvParams kp{num_accepted, draft_lens, seq_lens, block_tables, B, gamma_max, max_blocks,
+                  block_size, free_list, free_count, free_capacity, status};
+  const int grid = (B + sv::kKvThreads - 1) / sv::kKvThreads;
+  sv::sv_kv_rollback_kernel<<<grid, sv::kKvThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(kp);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 const char *sv_status_string(sv_status status) {
