@@ -166,6 +166,19 @@ SV_API sv_status spec_verify_diag(const void *target_logits, sv_dtype logits_dty
                            const sv_diag *diag);
 
 /*
+ * Self-test of failure detection without a GPU fault: launches one small
+ * kernel that waits, with a limit of `limit_us` microseconds (1 .. 10^6),
+ * for an mbarrier phase that nobody completes and for the device word
+ * `never_set` (the caller keeps it 0).  Both waits must give up: the kernel
+ * ORs SV_FAULT_TIMEOUT | 0x1 (the mbarrier wait) and 0x2 (the flag wait)
+ * into the device word `word` (the caller zeroes it) and ends; the context
+ * stays usable.  The verification kernels use the same waits with a ~2 s
+ * limit.  Asynchronous on `stream`.
+ */
+SV_API sv_status sv_selftest_wait_timeout(uint32_t *word, const uint32_t *never_set,
+                                          unsigned limit_us, sv_stream_t stream);
+
+/*
  * KV rollback hand-off after verification (P3 §5.4: the KV of the drafted
  * tokens is written first and marked tentative; after verification the cache
  * is cut at num_accepted and the blocks past the cut go back to the block

@@ -37,7 +37,8 @@ SV_FAULT_TIMEOUT = 0x10000
 
 # Every symbol include/spec_verify.h declares.
 EXPORTS = ("sv_workspace_bytes", "spec_verify", "spec_verify_diag",
-           "sv_last_error", "sv_status_string", "spec_verify_noalloc", "sv_kv_rollback")
+           "sv_last_error", "sv_status_string", "spec_verify_noalloc", "sv_kv_rollback",
+           "sv_selftest_wait_timeout")
 
 # Bits of the status word of sv_kv_rollback (include/spec_verify.h).
 SV_KV_FREE_LIST_FULL = 0x1
@@ -92,6 +93,8 @@ def load_library():
     lib.sv_last_error.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint32)]
     lib.sv_status_string.restype = ctypes.c_char_p
     lib.sv_status_string.argtypes = [_I]
+    lib.sv_selftest_wait_timeout.restype = _I
+    lib.sv_selftest_wait_timeout.argtypes = [_P, _P, ctypes.c_uint, _P]
     lib.sv_kv_rollback.restype = _I
     lib.sv_kv_rollback.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P]
     _lib = lib
@@ -255,6 +258,21 @@ def kv_rollback(num_accepted: torch.Tensor, seq_lens: torch.Tensor,
                             free_list.numel(), _ptr(status), _stream_handle(stream, dev))
     if rc != SV_OK:
         raise SpecVerifyError(rc, lib)
+
+
+def selftest_wait_timeout(limit_us: int = 1000, device="cuda") -> int:
+    """Run the bounded-wait self-test (``sv_selftest_wait_timeout``) and
+    return the status word it sets (synchronises)."""
+    lib = load_library()
+    dev = torch.device(device)
+    word = torch.zeros(1, dtype=torch.int32, device=dev)
+    never = torch.zeros(1, dtype=torch.int32, device=dev)
+    rc = lib.sv_selftest_wait_timeout(_ptr(word), _ptr(never), int(limit_us),
+                                      _stream_handle(None, dev))
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, lib)
+    torch.cuda.synchronize(dev)
+    return int(word.item()) & 0xFFFFFFFF
 
 
 def acceptance_stats(accept_hist) -> dict:

@@ -26,6 +26,30 @@
 #include "sv_verify.cuh"
 
 namespace sv {
+
+// Self-test of the bounded waits: an mbarrier phase that nobody completes
+// and a device flag that nobody sets, each waited for with a short limit.
+// Both must give up, set SV_FAULT_TIMEOUT and let the kernel end.
+__global__ void sv_selftest_wait_kernel(uint32_t *word, const uint32_t *never,
+                                        uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  if (!mbar_wait_slow(smem_addr(&bar), 0u, word, limit_ns)) atomicOr(word, 0x1u);
+  const uint64_t t0 = global_timer_ns();
+  while (ld_relaxed(never) == 0u) {
+    if (global_timer_ns() - t0 > limit_ns) {
+      atomicOr(word, SV_FAULT_TIMEOUT | 0x2u);
+      break;
+    }
+    __nanosleep(256);
+  }
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -215,6 +239,14 @@ sv_status sv_kv_rollback(const int32_t *num_accepted, const int32_t *draft_lens,
                   block_size, free_list, free_count, free_capacity, status};
   const int grid = (B + sv::kKvThreads - 1) / sv::kKvThreads;
   sv::sv_kv_rollback_kernel<<<grid, sv::kKvThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(kp);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+sv_status sv_selftest_wait_timeout(uint32_t *word, const uint32_t *never_set,
+                                    unsigned limit_us, sv_stream_t stream) {
+  if (!word || !never_set || limit_us == 0 || limit_us > 1000000u) return SV_ERR_INVALID_ARG;
+  sv::sv_selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      word, never_set, static_cast<uint64_t>(limit_us) * 1000u);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 

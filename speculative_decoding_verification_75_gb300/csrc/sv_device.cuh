@@ -88,12 +88,13 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return ok != 0;
 }
 
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
-                                            uint32_t *err) {
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint32_t *err,
+                                            uint64_t limit_ns = kWaitLimitNs) {
   const uint64_t t0 = global_timer_ns();
+  const uint32_t hint = limit_ns < 100000u ? static_cast<uint32_t>(limit_ns) : 100000u;
   for (uint32_t it = 1; it < (1u << 30); ++it) {
-    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) break;
+    if (mbar_try_wait_sleep(bar, parity, hint)) return true;
+    if (global_timer_ns() - t0 > limit_ns) break;
   }
   atomicOr(err, SV_FAULT_TIMEOUT);
   return false;

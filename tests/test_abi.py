@@ -93,3 +93,12 @@ def test_host_argument_errors_need_no_gpu(lib):
     assert _call(lib, B=0) == api.SV_OK            # empty batch: nothing to do
     assert _call(lib, g=0, ids=None, ua=None, B=0) == api.SV_OK
     assert lib.sv_last_error(None, None, None) == api.SV_ERR_INVALID_ARG
+
+
+def test_selftest_argument_errors_need_no_gpu(lib):
+    from speculative_decoding_verification_75_gb300 import api
+    p = ctypes.c_void_p(0x10000)  # never dereferenced: the call returns before any launch
+    assert lib.sv_selftest_wait_timeout(None, p, 1000, None) == api.SV_ERR_INVALID_ARG
+    assert lib.sv_selftest_wait_timeout(p, None, 1000, None) == api.SV_ERR_INVALID_ARG
+    assert lib.sv_selftest_wait_timeout(p, p, 0, None) == api.SV_ERR_INVALID_ARG
+    assert lib.sv_selftest_wait_timeout(p, p, 2_000_000, None) == api.SV_ERR_INVALID_ARG

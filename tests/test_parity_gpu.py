@@ -172,6 +172,20 @@ def test_all_greedy_batch_has_no_residual_work():
     assert (rc, word) == (api.SV_OK, 0)
 
 
+def test_bounded_waits_give_up_and_leave_the_context_usable():
+    """Failure detection without a GPU fault: an mbarrier phase nobody
+    completes and a flag nobody sets, each waited for with a 2 ms limit,
+    must time out with SV_FAULT_TIMEOUT; the next call then runs normally."""
+    import time
+    t0 = time.perf_counter()
+    word = api.selftest_wait_timeout(2000)
+    assert time.perf_counter() - t0 >= 0.004  # both waits ran to their limit
+    assert word == api.SV_FAULT_TIMEOUT | 0x1 | 0x2, hex(word)
+    case = make_case(workloads.workload("c1"), device=DEV)
+    rep, _, _ = check(case)
+    assert rep["exact"] + rep["borderline"] == 1
+
+
 def test_clean_call_reports_ok():
     case = make_case(workloads.workload("c1"), device=DEV)
     run_gpu(case)
