@@ -93,14 +93,16 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
 
 template <typename T, bool kTMA>
 sv_status launch_all(Params &p, cudaStream_t st, int dev, int nsm) {
-  static std::atomic<uint64_t> smem_done{0};
+  static std::atomic<uint64_t> smem_done{0}, smem_done_local{0};
   p.C1 = div_up(p.V, Tiling<T>::kRowChunk);
   p.C2 = div_up(p.V, Tiling<T>::kResChunk);
   p.nseg = p.C2 * Tiling<T>::kSegPerChunk;
 
-  auto *kv = sv_verify_kernel<T, kTMA>;
+  const bool local = p.B <= kLocalJobsB;
+  auto *kv = local ? sv_verify_kernel<T, kTMA, true> : sv_verify_kernel<T, kTMA, false>;
   const size_t smem = verify_smem_bytes();
-  if (ensure_smem(kv, smem, smem_done, dev) != cudaSuccess) return SV_ERR_CUDA;
+  if (ensure_smem(kv, smem, local ? smem_done_local : smem_done, dev) != cudaSuccess)
+    return SV_ERR_CUDA;
 
   sv_prepare_kernel<<<1, kPrepThreads, 0, st>>>(p);
   if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
