@@ -156,8 +156,7 @@ sv_status run(const void *logits, sv_dtype dtype, const int32_t *ids, const floa
   p.cs = reinterpret_cast<float *>(w + L.cs);
   p.k1_cnt = reinterpret_cast<uint32_t *>(w + L.k1_cnt);
   p.k2_cnt = reinterpret_cast<uint32_t *>(w + L.k2_cnt);
-  p.ready = reinterpret_cast<uint32_t *>(w + L.ready);
-  p.desc = reinterpret_cast<Desc *>(w + L.desc);
+  p.desc = reinterpret_cast<uint64_t *>(w + L.desc);
   p.jflag = reinterpret_cast<uint32_t *>(w + L.jflag);
   p.part1 = reinterpret_cast<Part *>(w + L.part1);
   p.csum = reinterpret_cast<float2 *>(w + L.csum);

@@ -13,6 +13,7 @@
 #include <cstdint>
 
 #include "spec_verify.h"
+#include "sv_device.cuh"
 
 namespace sv {
 
@@ -59,8 +60,8 @@ struct __align__(128) Header {  // 512 bytes: four 128-byte lines
 // b; job B + s searches the residual of descriptor slot s.
 constexpr uint32_t kJobWait = 0u, kJobDue = 1u, kJobNone = 2u;
 
-// ready[s]: descriptor slot s is reserved but not yet written / holds a row
-// to re-sample / holds nothing (its request turned out invalid).
+// State of descriptor slot s: reserved but not yet written / holds a row to
+// re-sample / holds nothing (its request turned out invalid).
 constexpr uint32_t kPending = 0u, kReadySample = 1u, kReadySkip = 2u;
 
 struct __align__(8) Part {  // per (row, chunk) partial statistics
@@ -79,10 +80,55 @@ struct __align__(16) Desc {
   float cs;     // log2(e) / T
   float u;      // sampling uniform
 };
+static_assert(sizeof(Desc) == 32, "eight 32-bit fields");
+
+// A descriptor slot holds the eight fields of a Desc in eight 64-bit words,
+// field i in the low half of word i and the slot's state in the high half.
+// The merge writes the words with relaxed 64-bit stores (each single-copy
+// atomic) and no fence; a reader takes the slot once every word carries the
+// state: a word can only show the state together with its own field, so no
+// release/acquire pair (a fence on each side, ~1-2 us under streaming load)
+// stands between a merge and the residual work it publishes.
+constexpr int kDescWords = 8;
+
+__device__ __forceinline__ void desc_publish(uint64_t *w, const Desc &d, uint32_t state) {
+  const uint32_t *f = reinterpret_cast<const uint32_t *>(&d);
+#pragma unroll
+  for (int i = 0; i < kDescWords; ++i)
+    st_relaxed64(w + i, (static_cast<uint64_t>(state) << 32) | f[i]);
+}
+
+// The slot's state as word 0 shows it (kPending until that word lands).
+__device__ __forceinline__ uint32_t desc_state(const uint64_t *w) {
+  return static_cast<uint32_t>(ld_relaxed64(w) >> 32);
+}
+
+// Waits (bounded) until every word of a kReadySample slot has landed.
+__device__ __forceinline__ bool desc_read(const uint64_t *w, Desc &d, uint32_t *err) {
+  uint32_t *f = reinterpret_cast<uint32_t *>(&d);
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    uint64_t v[kDescWords];
+#pragma unroll
+    for (int i = 0; i < kDescWords; ++i) v[i] = ld_relaxed64(w + i);
+    bool all = true;
+#pragma unroll
+    for (int i = 0; i < kDescWords; ++i) {
+      all = all && static_cast<uint32_t>(v[i] >> 32) == kReadySample;
+      f[i] = static_cast<uint32_t>(v[i]);
+    }
+    if (all) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, SV_FAULT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 
 // Byte offsets of each region inside the workspace.
 struct Layout {
-  size_t hdr, row_start, cs, k1_cnt, k2_cnt, ready, desc, jflag, part1, csum, ssum, total;
+  size_t hdr, row_start, cs, k1_cnt, k2_cnt, desc, jflag, part1, csum, ssum, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) {
@@ -115,8 +161,7 @@ inline Layout make_layout(int B, int gmax, int V) {
   L.cs = take(sizeof(float) * B);
   L.k1_cnt = take(sizeof(uint32_t) * B);
   L.k2_cnt = take(sizeof(uint32_t) * B);
-  L.ready = take(sizeof(uint32_t) * B);
-  L.desc = take(sizeof(Desc) * B);
+  L.desc = take(sizeof(uint64_t) * kDescWords * B);
   L.jflag = take(sizeof(uint32_t) * 2 * static_cast<size_t>(B));
   L.part1 = take(sizeof(Part) * rows * c1);
   L.csum = take(sizeof(float2) * B * c2);
@@ -146,8 +191,7 @@ struct Params {
   float *cs;         // [B] log2(e) / T (0: greedy)
   uint32_t *k1_cnt;  // [B] row-statistics chunks completed
   uint32_t *k2_cnt;  // [B] residual chunks completed
-  uint32_t *ready;   // [B] kPending / kReadySample / kReadySkip per slot
-  Desc *desc;        // [B] rows to re-sample, in reservation (merge) order
+  uint64_t *desc;    // [B][kDescWords] rows to re-sample, in reservation (merge) order
   uint32_t *jflag;   // [2B] kJobWait / kJobDue / kJobNone per job
   Part *part1;
   float2 *csum;      // [slot][C2] residual and p sums per chunk

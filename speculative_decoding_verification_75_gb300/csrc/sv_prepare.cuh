@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prepare_kernel(Params p) {
       p.cs[b] = (t > 0.f) ? kLog2e / t : 0.f;
       p.k1_cnt[b] = 0u;
       p.k2_cnt[b] = 0u;
-      p.ready[b] = kPending;
+      for (int i = 0; i < kDescWords; ++i) p.desc[static_cast<size_t>(b) * kDescWords + i] = 0ull;
       p.jflag[b] = nr == 0 ? kJobNone : kJobWait;  // no merge without rows
       p.jflag[p.B + b] = kJobWait;
       if (nr == 0) {

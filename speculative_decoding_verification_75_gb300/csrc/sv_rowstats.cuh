@@ -355,7 +355,7 @@ __device__ __noinline__ void merge_request(const Params &p, int b, int nr, float
       atomicOr(&p.hdr->err, bad);
       if (!greedy) {  // the reserved slot holds nothing: no residual, no search
         p.jflag[p.B + pos] = kJobNone;
-        st_release(&p.ready[pos], kReadySkip);
+        desc_publish(p.desc + static_cast<size_t>(pos) * kDescWords, Desc{}, kReadySkip);
       }
       if (dg.accept_hist) atomicAdd(dg.accept_hist + p.gmax + 1, 1);
       count_merged(p);
@@ -370,8 +370,8 @@ __device__ __noinline__ void merge_request(const Params &p, int b, int nr, float
     xk = -1;
   }
   if (lane == 0 && !greedy) {
-    // Publish first: the slot's residual chunks become claimable once the
-    // flag is seen; the release orders the descriptor before it.
+    // Publish first: the slot's residual chunks become claimable once its
+    // words are seen (no fence: each word carries the state).
     Desc d;
     d.b = b;
     d.k = k;
@@ -381,8 +381,7 @@ __device__ __noinline__ void merge_request(const Params &p, int b, int nr, float
     d.inv_s = 1.f / sk;
     d.cs = cs;
     d.u = us;
-    p.desc[pos] = d;
-    st_release(&p.ready[pos], kReadySample);
+    desc_publish(p.desc + static_cast<size_t>(pos) * kDescWords, d, kReadySample);
   }
   for (int i = lane; i < R; i += 32) {
     int tk = -1;

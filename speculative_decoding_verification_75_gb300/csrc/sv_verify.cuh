@@ -175,6 +175,17 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
   uint32_t *err = &p.hdr->err;
   auto row_start = [&](int b) { return smem_req ? row_start_s[b] : ld_cg(p.row_start + b); };
   auto scale = [&](int b) { return smem_req ? cs_s[b] : ld_cg(p.cs + b); };
+  // Warp-wide: the search of slot sl, once lane 0 has read its descriptor.
+  auto search_slot = [&](int sl) {
+    Desc d{};
+    bool ok = true;
+    if (lane == 0) ok = desc_read(p.desc + static_cast<size_t>(sl) * kDescWords, d, err);
+    if (!__shfl_sync(kFull, ok ? 1 : 0, 0)) return;
+    uint32_t *f = reinterpret_cast<uint32_t *>(&d);
+#pragma unroll
+    for (int i = 0; i < kDescWords; ++i) f[i] = __shfl_sync(kFull, f[i], 0);
+    search_request<T, kTMA>(p, d, sl, lane);
+  };
 
   if (warp == kWarpCounter) {
     // --------------------------------------------------- counter warp ----
@@ -214,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
           if (kind == 0) {
             merge_request<T>(p, id, row_start(id + 1) - row_start(id), scale(id), lane);
           } else {
-            search_request<T, kTMA>(p, ld_cg(p.desc + id), id, lane);
+            search_slot(id);
           }
         }
       }
@@ -265,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
         const int rows = row_start(id + 1) - row_start(id);
         merge_request<T>(p, id, rows, scale(id), lane);
       } else {
-        search_request<T, kTMA>(p, ld_cg(p.desc + (id - p.B)), id - p.B, lane);
+        search_slot(id - p.B);
       }
     }
     return;
@@ -301,12 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
     auto await_slot = [&](uint32_t sl) -> uint32_t {
       if (sl >= static_cast<uint32_t>(p.B)) return 0u;  // at most one slot per request
       const uint64_t t0 = global_timer_ns();
-      for (;;) {  // relaxed polls; one acquire fence once a flag is seen
-        const uint32_t f = ld_relaxed(p.ready + sl);
-        if (f != kPending) {
-          fence_acq_rel();
-          return f;
-        }
+      for (;;) {  // relaxed polls of the slot's first word
+        const uint32_t f = desc_state(p.desc + static_cast<size_t>(sl) * kDescWords);
+        if (f != kPending) return f;
         // All merged: every reservation is visible, b_reserved is final.
         if (ld_relaxed(&p.hdr->all_merged) != 0u) {
           fence_acq_rel();
@@ -327,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
         const uint2 bc = ld_relaxed2(&p.hdr->b_next);  // {b_next, b_reserved}
         const uint32_t sl = bc.x / C2;
         if (sl < bc.y) {
-          const uint32_t f = ld_relaxed(p.ready + sl);
+          const uint32_t f = desc_state(p.desc + static_cast<size_t>(sl) * kDescWords);
           const uint32_t s_end = (sl + 1) * C2;
           if (f == kReadySkip) {
             atomicMax(&p.hdr->b_next, s_end);
@@ -336,10 +344,12 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
           if (f == kReadySample) {
             const uint32_t want = min(bc.x + rt, s_end);
             if (atomicCAS(&p.hdr->b_next, bc.x, want) == bc.x) {
-              fence_acq_rel();  // the slot's flag was seen: its descriptor is written
+              Desc d;
+              ok = ok && desc_read(p.desc + static_cast<size_t>(sl) * kDescWords, d, err);
               const int c0 = static_cast<int>(bc.x - sl * C2);
-              push(Claim{1, 0u, 0u, static_cast<int>(sl), c0, c0 + static_cast<int>(want - bc.x),
-                         {0, 0}, ld_cg(p.desc + sl)});
+              if (ok)
+                push(Claim{1, 0u, 0u, static_cast<int>(sl), c0,
+                           c0 + static_cast<int>(want - bc.x), {0, 0}, d});
               continue;
             }
           }
@@ -364,9 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
         }
         const uint32_t seg_end = min(r_end, s_end);
         if (f == kReadySample) {
+          Desc d;
+          ok = ok && desc_read(p.desc + static_cast<size_t>(sl) * kDescWords, d, err);
           const int c0 = static_cast<int>(it - sl * C2);
-          push(Claim{1, 0u, 0u, static_cast<int>(sl), c0, c0 + static_cast<int>(seg_end - it),
-                     {0, 0}, ld_cg(p.desc + sl)});
+          if (ok)
+            push(Claim{1, 0u, 0u, static_cast<int>(sl), c0,
+                       c0 + static_cast<int>(seg_end - it), {0, 0}, d});
         } else {
           atomicMax(&p.hdr->b_next, s_end);  // an unused slot: pass it over
         }
