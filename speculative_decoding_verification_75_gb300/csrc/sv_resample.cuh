@@ -23,14 +23,16 @@ namespace sv {
 // p_j of the target softmax and r_j = (p_j - q_j)_+, as a fixed sequence of
 // correctly rounded operations: the packed fp32x2 forms in the streaming pass
 // and these scalar forms in the search give identical values.
-__device__ __forceinline__ float target_p(float x, float m, float cs, float inv_s) {
-  return __fmul_rn(ex2(__fmul_rn(__fsub_rn(x, m), cs)), inv_s);
+// p(x) = exp2(x * cs - o) / s, with o = fl(m * cs) for the row maximum m and
+// s the row's sum relative to the same offset (the merge keeps it so).
+__device__ __forceinline__ float target_p(float x, float nego, float cs, float inv_s) {
+  return __fmul_rn(ex2(__fmaf_rn(x, cs, nego)), inv_s);
 }
 __device__ __forceinline__ float resid(float p, float q) {
   return fmaxf(__fsub_rn(p, q), 0.f);
 }
-__device__ __forceinline__ float2 target_p2(float2 x, float2 negm, float2 cs2, float2 inv2) {
-  const float2 t = __fmul2_rn(__fadd2_rn(x, negm), cs2);
+__device__ __forceinline__ float2 target_p2(float2 x, float2 nego, float2 cs2, float2 inv2) {
+  const float2 t = __ffma2_rn(x, cs2, nego);
   return __fmul2_rn(make_float2(ex2(t.x), ex2(t.y)), inv2);
 }
 
@@ -118,6 +120,7 @@ __device__ __forceinline__ int search_segment(const Params &p, const Desc &d, in
                                               float carry, float target, bool use_p,
                                               int lane) {
   const T *row = static_cast<const T *>(p.logits) + static_cast<size_t>(d.slot) * p.V;
+  const float nego = -__fmul_rn(d.m, d.cs);  // the row's exponent offset, negated
   const int l0 = 32 * lane;
   float x[32], q[32];
   if (kVec && l0 + 32 <= n) {
@@ -163,7 +166,7 @@ __device__ __forceinline__ int search_segment(const Params &p, const Desc &d, in
   float tot = 0.f;
 #pragma unroll
   for (int t = 0; t < 32; ++t) {
-    const float pj = target_p(x[t], d.m, d.cs, d.inv_s);
+    const float pj = target_p(x[t], nego, d.cs, d.inv_s);
     w[t] = (l0 + t < n) ? (use_p ? pj : resid(pj, q[t])) : 0.f;
     tot += w[t];
   }
@@ -349,7 +352,8 @@ __device__ __forceinline__ float2 chunk_resid(const Params &p, const Desc &d, in
   const float *qrow =
       has_q ? p.q + (static_cast<size_t>(d.b) * p.gmax + d.k) * p.V : nullptr;
   const float *sq = reinterpret_cast<const float *>(stage + kChunk * sizeof(T));
-  const float2 negm = make_float2(-d.m, -d.m), cs2 = make_float2(d.cs, d.cs);
+  const float nego1 = -__fmul_rn(d.m, d.cs);  // the row's exponent offset, negated
+  const float2 nego = make_float2(nego1, nego1), cs2 = make_float2(d.cs, d.cs);
   const float2 inv2 = make_float2(d.inv_s, d.inv_s), zero2 = make_float2(0.f, 0.f);
   const bool onehot = d.tok >= 0 && !has_q;
   const int nsg = (ne + kSeg - 1) / kSeg;
@@ -392,8 +396,8 @@ __device__ __forceinline__ float2 chunk_resid(const Params &p, const Desc &d, in
             q01 = make_float2(qs[0], qs[1]);
             q23 = make_float2(qs[2], qs[3]);
           }
-          const float2 p01 = target_p2(x01, negm, cs2, inv2);
-          const float2 p23 = target_p2(x23, negm, cs2, inv2);
+          const float2 p01 = target_p2(x01, nego, cs2, inv2);
+          const float2 p23 = target_p2(x23, nego, cs2, inv2);
           const float2 d01 = __fadd2_rn(p01, q01), d23 = __fadd2_rn(p23, q23);
           float r[4] = {fmaxf(d01.x, 0.f), fmaxf(d01.y, 0.f), fmaxf(d23.x, 0.f),
                         fmaxf(d23.y, 0.f)};

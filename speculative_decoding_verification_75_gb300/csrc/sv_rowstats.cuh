@@ -6,9 +6,13 @@
 // q clamped at 1e-10, accepted = u < a, cumprod prefix = first rejection.
 //
 // A consumer warp reduces one chunk held in shared memory: pass A takes the
-// maximum (packed bf16x2 max), pass B the sum of exp2((l - max) * log2(e)/T)
-// with packed fp32x2 arithmetic (greedy rows instead find the lowest index of
-// the maximum).  p itself is never stored: only (max, sum) per chunk reaches
+// maximum m (packed bf16x2 max), pass B the sum of exp2(l * cs - o) with
+// cs = log2(e)/T and the offset o = fl(m * cs), one packed fp32x2 fma per
+// pair of logits (greedy rows instead find the lowest index of the maximum).
+// The fma forms l * cs - o exactly and rounds once, so each exponent is
+// accurate relative to its own size, and whoever combines the statistics
+// recomputes o from m: the sum stands for exp2((l - m) * cs) summed, times
+// the exact factor exp2(m * cs - o).  p itself is never stored: only (max, sum) per chunk reaches
 // global memory.  When every chunk of a request is done, one warp merges the
 // chunk statistics in chunk order, checks the request's inputs, gathers
 // p(x_i) and q(x_i), runs the accept test for all positions with one ballot,
@@ -24,8 +28,11 @@ namespace sv {
 
 struct ChunkStat {
   float m;  // maximum logit of the chunk
-  float v;  // sum of exp2((l - m) * cs), or the argmax bits for greedy rows
+  float v;  // sum of exp2(l * cs - offset(m, cs)), or the argmax bits for greedy rows
 };
+
+// The exponent offset of a chunk (or row) whose maximum is m.
+__device__ __forceinline__ float offset(float m, float cs) { return __fmul_rn(m, cs); }
 
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
   __nv_bfloat162 r = __hmax2(*reinterpret_cast<__nv_bfloat162 *>(&a),
@@ -33,9 +40,9 @@ __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t *>(&r);
 }
 
-// exp2((x - m) * cs) for a pair, packed fp32x2 arithmetic.
-__device__ __forceinline__ float2 exp_pair(float2 x, float2 negm, float2 cs2) {
-  const float2 t = __fmul2_rn(__fadd2_rn(x, negm), cs2);
+// exp2(x * cs - o) for a pair (nego = -o), one packed fp32x2 fma.
+__device__ __forceinline__ float2 exp_pair(float2 x, float2 nego, float2 cs2) {
+  const float2 t = __ffma2_rn(x, cs2, nego);
   return make_float2(ex2(t.x), ex2(t.y));
 }
 
@@ -54,15 +61,16 @@ __device__ __forceinline__ ChunkStat chunk_stats_smem(const __nv_bfloat16 *stage
   ChunkStat r{m, 0.f};
   if (cs != 0.f) {
     if (m == -INFINITY) return r;  // fully masked chunk contributes nothing
-    const float2 negm = make_float2(-m, -m), cs2 = make_float2(cs, cs);
+    const float o = offset(m, cs);
+    const float2 nego = make_float2(-o, -o), cs2 = make_float2(cs, cs);
     float2 a0 = make_float2(0.f, 0.f), a1 = a0;
 #pragma unroll 4
     for (int i = lane; i < nvec; i += 32) {
       const uint4 x = v[i];
-      a0 = __fadd2_rn(a0, exp_pair(make_float2(bf16_lo(x.x), bf16_hi(x.x)), negm, cs2));
-      a1 = __fadd2_rn(a1, exp_pair(make_float2(bf16_lo(x.y), bf16_hi(x.y)), negm, cs2));
-      a0 = __fadd2_rn(a0, exp_pair(make_float2(bf16_lo(x.z), bf16_hi(x.z)), negm, cs2));
-      a1 = __fadd2_rn(a1, exp_pair(make_float2(bf16_lo(x.w), bf16_hi(x.w)), negm, cs2));
+      a0 = __fadd2_rn(a0, exp_pair(make_float2(bf16_lo(x.x), bf16_hi(x.x)), nego, cs2));
+      a1 = __fadd2_rn(a1, exp_pair(make_float2(bf16_lo(x.y), bf16_hi(x.y)), nego, cs2));
+      a0 = __fadd2_rn(a0, exp_pair(make_float2(bf16_lo(x.z), bf16_hi(x.z)), nego, cs2));
+      a1 = __fadd2_rn(a1, exp_pair(make_float2(bf16_lo(x.w), bf16_hi(x.w)), nego, cs2));
     }
     r.v = warp_sum((a0.x + a0.y) + (a1.x + a1.y));
     return r;
@@ -108,13 +116,14 @@ __device__ __forceinline__ ChunkStat chunk_stats_smem(const float *stage, int ne
   ChunkStat r{m, 0.f};
   if (cs != 0.f) {
     if (m == -INFINITY) return r;
-    const float2 negm = make_float2(-m, -m), cs2 = make_float2(cs, cs);
+    const float o = offset(m, cs);
+    const float2 nego = make_float2(-o, -o), cs2 = make_float2(cs, cs);
     float2 a0 = make_float2(0.f, 0.f), a1 = a0;
 #pragma unroll 4
     for (int i = lane; i < nvec; i += 32) {
       const float4 x = v[i];
-      a0 = __fadd2_rn(a0, exp_pair(make_float2(x.x, x.y), negm, cs2));
-      a1 = __fadd2_rn(a1, exp_pair(make_float2(x.z, x.w), negm, cs2));
+      a0 = __fadd2_rn(a0, exp_pair(make_float2(x.x, x.y), nego, cs2));
+      a1 = __fadd2_rn(a1, exp_pair(make_float2(x.z, x.w), nego, cs2));
     }
     r.v = warp_sum((a0.x + a0.y) + (a1.x + a1.y));
     return r;
@@ -151,9 +160,9 @@ __device__ __forceinline__ ChunkStat chunk_stats_global(const T *row, int e0, in
   ChunkStat r{m, 0.f};
   if (cs != 0.f) {
     if (m == -INFINITY) return r;
+    const float o = offset(m, cs);
     float s = 0.f;
-    for (int j = lane; j < ne; j += 32)
-      s += ex2(__fmul_rn(__fsub_rn(Elem<T>::load(row, e0 + j), m), cs));
+    for (int j = lane; j < ne; j += 32) s += ex2(__fmaf_rn(Elem<T>::load(row, e0 + j), cs, -o));
     r.v = warp_sum(s);
     return r;
   }
@@ -179,10 +188,10 @@ __device__ __forceinline__ int half0_len(int ne) { return min(ne, ((ne + 15) >> 
 // 0).  Greedy rows keep the lowest index of the maximum.
 __device__ __forceinline__ ChunkStat combine_halves(ChunkStat a, ChunkStat b, float cs) {
   if (cs == 0.f) return (b.m > a.m) ? b : a;
-  const float m = fmaxf(a.m, b.m);
+  const float m = fmaxf(a.m, b.m), o = offset(m, cs);
   float s = 0.f;
-  if (a.m != -INFINITY) s = __fmul_rn(a.v, ex2(__fmul_rn(__fsub_rn(a.m, m), cs)));
-  if (b.m != -INFINITY) s = __fadd_rn(s, __fmul_rn(b.v, ex2(__fmul_rn(__fsub_rn(b.m, m), cs))));
+  if (a.m != -INFINITY) s = __fmul_rn(a.v, ex2(__fsub_rn(offset(a.m, cs), o)));
+  if (b.m != -INFINITY) s = __fadd_rn(s, __fmul_rn(b.v, ex2(__fsub_rn(offset(b.m, cs), o))));
   return ChunkStat{m, s};
 }
 
@@ -274,24 +283,29 @@ __device__ __noinline__ void merge_request(const Params &p, int b, int nr, float
               m = q[tj].m;
               am = __float_as_int(q[tj].v);
             }
-          } else if (q[tj].m > m) {
-            s = __fadd_rn(__fmul_rn(s, ex2(__fmul_rn(__fsub_rn(m, q[tj].m), cs))), q[tj].v);
+          } else if (q[tj].m > m) {  // sums are kept relative to offset(m)
+            s = __fadd_rn(__fmul_rn(s, ex2(__fsub_rn(offset(m, cs), offset(q[tj].m, cs)))),
+                          q[tj].v);
             m = q[tj].m;
           } else if (q[tj].m != -INFINITY) {
-            s = __fadd_rn(s, __fmul_rn(q[tj].v, ex2(__fmul_rn(__fsub_rn(q[tj].m, m), cs))));
+            s = __fadd_rn(s, __fmul_rn(q[tj].v, ex2(__fsub_rn(offset(q[tj].m, cs), offset(m, cs)))));
           }
         }
       }
       if (greedy) s = 1.f;
       else if (!(isfinite(m) && isfinite(s))) bad |= SV_BAD_NORMALISER;
       if (dg.row_max) dg.row_max[static_cast<size_t>(b) * R + i] = m;
-      if (dg.row_sum) dg.row_sum[static_cast<size_t>(b) * R + i] = s;
+      // The normaliser as defined, sum exp2((l - m) * cs): the stored sum
+      // times exp2(offset(m) - m * cs), whose exponent one fma forms exactly.
+      if (dg.row_sum)
+        dg.row_sum[static_cast<size_t>(b) * R + i] =
+            greedy ? s : __fmul_rn(s, ex2(-__fmaf_rn(m, cs, -offset(m, cs))));
       if (dg.row_argmax) dg.row_argmax[static_cast<size_t>(b) * R + i] = am;
 
       if (draft) {
         // Accept test for draft position i.
         const float P = greedy ? ((xc == am) ? 1.f : 0.f)
-                               : ex2(__fmul_rn(__fsub_rn(lx, m), cs)) / s;
+                               : ex2(__fmaf_rn(lx, cs, -offset(m, cs))) / s;
         const float a = fminf(1.f, P / fmaxf(qraw, kQFloor));
         f = u < a;
         if (dg.p_tok) dg.p_tok[pi] = P;
