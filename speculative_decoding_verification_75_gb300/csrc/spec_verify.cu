@@ -104,8 +104,8 @@ sv_status launch_all(Params &p, cudaStream_t st, int dev, int nsm) {
   if (ensure_smem(kv, smem, local ? smem_done_local : smem_done, dev) != cudaSuccess)
     return SV_ERR_CUDA;
 
-  sv_prepare_kernel<<<1, kPrepThreads, 0, st>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  if (launch_pdl(sv_prepare_kernel, dim3(1), dim3(kPrepThreads), 0, st, p) != cudaSuccess)
+    return SV_ERR_CUDA;
 
   const long long max_items = static_cast<long long>(p.B) * (p.gmax + 1) * p.C1;
   const int grid = static_cast<int>(max_items < nsm ? max_items : nsm);

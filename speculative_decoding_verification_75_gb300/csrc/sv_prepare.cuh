@@ -1,6 +1,6 @@
 // sv_prepare.cuh -- kernel 0: per-call set-up of the workspace.
 //
-// One CTA walks the batch 1024 requests at a time: it writes each request's
+// One CTA walks the batch 256 requests at a time: it writes each request's
 // first flat row (an exclusive scan of g_b + 1) and softmax scale log2(e)/T,
 // clears the request's arrival counters and descriptor flag, and writes the
 // -1 outputs of requests whose draft length is invalid (they get no rows).
@@ -14,7 +14,10 @@
 
 namespace sv {
 
-constexpr int kPrepThreads = 1024;
+// Small enough to sit beside a persistent CTA on one SM (registers, threads),
+// so that it can be resident while the previous step's grid finishes.
+constexpr int kPrepThreads = 256;
+constexpr int kPrepWarps = kPrepThreads / 32;
 
 __device__ void fill_bad_request(const Params &p, int b) {
   const int R = p.gmax + 1;
@@ -39,8 +42,12 @@ __device__ void fill_bad_request(const Params &p, int b) {
 }
 
 __global__ void __launch_bounds__(kPrepThreads) sv_prepare_kernel(Params p) {
-  // The persistent kernel may start its prologue now; it waits for this
-  // grid's completion before it reads anything written here.
+  // Launched as a programmatic dependent: it may be resident before the
+  // previous grid on the stream has finished, so it waits for that grid's
+  // completion (and memory) before touching anything.  The persistent
+  // kernel may then start its prologue; it waits for this grid's completion
+  // before it reads anything written here.
+  pdl_wait();
   pdl_launch_dependents();
   __shared__ int warp_tot[32];
   __shared__ int carry, valid;
@@ -84,7 +91,7 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prepare_kernel(Params p) {
     if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-      int w = warp_tot[lane];
+      int w = lane < kPrepWarps ? warp_tot[lane] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int n = __shfl_up_sync(kFull, w, o);
@@ -95,7 +102,7 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prepare_kernel(Params p) {
     __syncthreads();
     if (b < p.B) p.row_start[b] = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + incl - nr;
     __syncthreads();
-    if (tid == 0) carry += warp_tot[31];
+    if (tid == 0) carry += warp_tot[kPrepWarps - 1];
     __syncthreads();
   }
   if (tid == 0) {

@@ -164,6 +164,9 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
     fence_mbar_init();
   }
   pdl_wait();  // kernel 0's row offsets, scales and reset counters
+  // The next step's kernel 0 may become resident beside this CTA; it waits
+  // for this grid's completion before it touches the workspace.
+  pdl_launch_dependents();
   const bool smem_req = p.B <= kSmemReq;
   if (smem_req) {
     for (int i = threadIdx.x; i <= p.B; i += kThreads) row_start_s[i] = ld_cg(p.row_start + i);
