@@ -267,29 +267,43 @@ __device__ __noinline__ void merge_request(const Params &p, int b, int nr, float
         if (!x_ok) bad |= SV_BAD_TOKEN;
         if (!valid_uniform(u)) bad |= SV_BAD_U_ACCEPT;
       }
-      // Online merge of the chunk statistics in chunk order (one batch
-      // covers a bf16 row of up to 196608 entries; longer rows take more).
+      // Merge of the chunk statistics, a batch at a time (one batch covers a
+      // bf16 row of up to 196608 entries; longer rows take more): the
+      // batch's maximum first, then its chunks' sums against that offset as
+      // independent terms, then the batch into the running pair.  Sums are
+      // kept relative to offset(m).
       for (int c0 = 0; c0 < p.C1; c0 += kMergeBatch) {
         if (c0 > 0) {
 #pragma unroll
           for (int tj = 0; tj < kMergeBatch; ++tj)
             q[tj] = (c0 + tj < p.C1) ? ld_cg(pp + c0 + tj) : Part{-INFINITY, 0.f};
         }
+        if (greedy) {
 #pragma unroll
-        for (int tj = 0; tj < kMergeBatch; ++tj) {
-          if (c0 + tj >= p.C1) break;
-          if (greedy) {
+          for (int tj = 0; tj < kMergeBatch; ++tj) {
+            if (c0 + tj >= p.C1) break;
             if (q[tj].m > m || am < 0) {
               m = q[tj].m;
               am = __float_as_int(q[tj].v);
             }
-          } else if (q[tj].m > m) {  // sums are kept relative to offset(m)
-            s = __fadd_rn(__fmul_rn(s, ex2(__fsub_rn(offset(m, cs), offset(q[tj].m, cs)))),
-                          q[tj].v);
-            m = q[tj].m;
-          } else if (q[tj].m != -INFINITY) {
-            s = __fadd_rn(s, __fmul_rn(q[tj].v, ex2(__fsub_rn(offset(q[tj].m, cs), offset(m, cs)))));
           }
+          continue;
+        }
+        float bm = -INFINITY;
+#pragma unroll
+        for (int tj = 0; tj < kMergeBatch; ++tj) bm = fmaxf(bm, q[tj].m);  // padding is -inf
+        if (bm == -INFINITY) continue;  // every chunk of the batch masked
+        const float ob = offset(bm, cs);
+        float bs = 0.f;
+#pragma unroll
+        for (int tj = 0; tj < kMergeBatch; ++tj)
+          if (q[tj].m != -INFINITY)
+            bs = __fadd_rn(bs, __fmul_rn(q[tj].v, ex2(__fsub_rn(offset(q[tj].m, cs), ob))));
+        if (bm > m) {
+          s = __fadd_rn(__fmul_rn(s, ex2(__fsub_rn(offset(m, cs), ob))), bs);
+          m = bm;
+        } else {
+          s = __fadd_rn(s, __fmul_rn(bs, ex2(__fsub_rn(ob, offset(m, cs)))));
         }
       }
       if (greedy) s = 1.f;

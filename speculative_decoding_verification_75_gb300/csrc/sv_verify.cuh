@@ -210,16 +210,20 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
       k += nb;
       bool last = false;
       if (e.kind >= 0) {
-        __threadfence();  // the run's results (observed by the producer) go first
         uint32_t *cnt = e.kind == 0 ? p.k1_cnt + e.id : p.k2_cnt + e.id;
         const uint32_t total = e.kind == 0 ? static_cast<uint32_t>(e.nr * p.C1)
                                            : static_cast<uint32_t>(p.C2);
-        last = atomicAdd(cnt, static_cast<uint32_t>(e.count)) + e.count == total;
-        if (last) fence_acq_rel();  // acquire every other run's results
+        // Release: the run's results (observed by the producer); acquire:
+        // every earlier run's, when this one completes the count.
+        last = atomic_add_acq_rel(cnt, static_cast<uint32_t>(e.count)) + e.count == total;
       }
-      // Job due: the merge of request id, or the search of slot id.  The
-      // fence above orders every run's results before this flag.
-      if (last) st_relaxed(p.jflag + (e.kind == 0 ? 0 : p.B) + e.id, kLocal ? kJobNone : kJobDue);
+      // Job due: the merge of request id, or the search of slot id; the
+      // release carries every run's results to the job warp that sees it.
+      if (last) {
+        uint32_t *flag = p.jflag + (e.kind == 0 ? 0 : p.B) + e.id;
+        if (kLocal) st_relaxed(flag, kJobNone);
+        else st_release(flag, kJobDue);
+      }
       if constexpr (kLocal) {  // run the completed jobs here, one after another
         for (unsigned lm = __ballot_sync(kFull, last); lm; lm &= lm - 1) {
           const int src = __ffs(lm) - 1;
