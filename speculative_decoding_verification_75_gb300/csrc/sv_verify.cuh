@@ -178,17 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
   uint32_t *err = &p.hdr->err;
   auto row_start = [&](int b) { return smem_req ? row_start_s[b] : ld_cg(p.row_start + b); };
   auto scale = [&](int b) { return smem_req ? cs_s[b] : ld_cg(p.cs + b); };
-  // Warp-wide: the search of slot sl, once lane 0 has read its descriptor.
-  auto search_slot = [&](int sl) {
-    Desc d{};
-    bool ok = true;
-    if (lane == 0) ok = desc_read(p.desc + static_cast<size_t>(sl) * kDescWords, d, err);
-    if (!__shfl_sync(kFull, ok ? 1 : 0, 0)) return;
-    uint32_t *f = reinterpret_cast<uint32_t *>(&d);
-#pragma unroll
-    for (int i = 0; i < kDescWords; ++i) f[i] = __shfl_sync(kFull, f[i], 0);
-    search_request<T, kTMA>(p, d, sl, lane);
-  };
+  auto search_slot = [&](int sl) { search_request<T, kTMA>(p, sl, lane); };
 
   if (warp == kWarpCounter) {
     // --------------------------------------------------- counter warp ----
