@@ -245,11 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
         h = atomicAdd(&p.hdr->jq_head, 1u);
         if (h >= njobs) state = 3;
         const uint64_t t0 = global_timer_ns();
-        // Relaxed polls; one acquire fence once a flag is seen.
+        // Acquire polls of the flag (no separate fence once it is seen).
         while (state == 0) {
-          const uint32_t f = ld_relaxed(p.jflag + h);
+          const uint32_t f = ld_acquire(p.jflag + h);  // pairs with the counter's release
           if (f == kJobDue) {
-            fence_acq_rel();
             state = 1;
           } else if (f == kJobNone) {
             state = 2;
