@@ -98,9 +98,24 @@ __device__ __forceinline__ void desc_publish(uint64_t *w, const Desc &d, uint32_
     st_relaxed64(w + i, (static_cast<uint64_t>(state) << 32) | f[i]);
 }
 
-// The slot's state as word 0 shows it (kPending until that word lands).
-__device__ __forceinline__ uint32_t desc_state(const uint64_t *w) {
-  return static_cast<uint32_t>(ld_relaxed64(w) >> 32);
+
+// One poll of a slot: all eight words in one round trip.  kReadySample only
+// once every word carries it (d is then complete), kReadySkip as word 0
+// shows it, else kPending.
+__device__ __forceinline__ uint32_t desc_poll(const uint64_t *w, Desc &d) {
+  uint32_t *f = reinterpret_cast<uint32_t *>(&d);
+  uint64_t v[kDescWords];
+#pragma unroll
+  for (int i = 0; i < kDescWords; ++i) v[i] = ld_relaxed64(w + i);
+  const uint32_t s0 = static_cast<uint32_t>(v[0] >> 32);
+  if (s0 != kReadySample) return s0;
+  bool all = true;
+#pragma unroll
+  for (int i = 0; i < kDescWords; ++i) {
+    all = all && static_cast<uint32_t>(v[i] >> 32) == kReadySample;
+    f[i] = static_cast<uint32_t>(v[i]);
+  }
+  return all ? kReadySample : kPending;
 }
 
 // Waits (bounded) until every word of a kReadySample slot has landed.

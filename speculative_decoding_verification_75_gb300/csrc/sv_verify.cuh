@@ -303,13 +303,14 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
     uint32_t k = 0;
     bool ok = true;
     auto push = [&](const Claim &c) { ok = ok && svc_push(clq, k++, c, err); };
-    // Slot s: kReadySample or kReadySkip once written; 0 when it will never
-    // be (every request merged, fewer slots reserved) or on a timeout.
-    auto await_slot = [&](uint32_t sl) -> uint32_t {
+    // Slot s: kReadySample (d holds its descriptor) or kReadySkip once
+    // written; 0 when it will never be (every request merged, fewer slots
+    // reserved) or on a timeout.
+    auto await_slot = [&](uint32_t sl, Desc &d) -> uint32_t {
       if (sl >= static_cast<uint32_t>(p.B)) return 0u;  // at most one slot per request
       const uint64_t t0 = global_timer_ns();
-      for (;;) {  // relaxed polls of the slot's first word
-        const uint32_t f = desc_state(p.desc + static_cast<size_t>(sl) * kDescWords);
+      for (;;) {  // relaxed polls of the slot's eight words
+        const uint32_t f = desc_poll(p.desc + static_cast<size_t>(sl) * kDescWords, d);
         if (f != kPending) return f;
         // All merged: every reservation is visible, b_reserved is final.
         if (ld_relaxed(&p.hdr->all_merged) != 0u) {
@@ -331,7 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
         const uint2 bc = ld_relaxed2(&p.hdr->b_next);  // {b_next, b_reserved}
         const uint32_t sl = bc.x / C2;
         if (sl < bc.y) {
-          const uint32_t f = desc_state(p.desc + static_cast<size_t>(sl) * kDescWords);
+          Desc d;
+          const uint32_t f = desc_poll(p.desc + static_cast<size_t>(sl) * kDescWords, d);
           const uint32_t s_end = (sl + 1) * C2;
           if (f == kReadySkip) {
             atomicMax(&p.hdr->b_next, s_end);
@@ -339,13 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
           }
           if (f == kReadySample) {
             const uint32_t want = min(bc.x + rt, s_end);
-            if (atomicCAS(&p.hdr->b_next, bc.x, want) == bc.x) {
-              Desc d;
-              ok = ok && desc_read(p.desc + static_cast<size_t>(sl) * kDescWords, d, err);
+            if (atomicCAS(&p.hdr->b_next, bc.x, want) == bc.x) {  // d is complete
               const int c0 = static_cast<int>(bc.x - sl * C2);
-              if (ok)
-                push(Claim{1, 0u, 0u, static_cast<int>(sl), c0,
-                           c0 + static_cast<int>(want - bc.x), {0, 0}, d});
+              push(Claim{1, 0u, 0u, static_cast<int>(sl), c0, c0 + static_cast<int>(want - bc.x),
+                         {0, 0}, d});
               continue;
             }
           }
@@ -363,19 +362,17 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
       const uint32_t r = atomicAdd(&p.hdr->b_next, rt);
       for (uint32_t it = r, r_end = r + rt; ok && it < r_end;) {
         const uint32_t sl = it / C2, s_end = (sl + 1) * C2;
-        const uint32_t f = await_slot(sl);
+        Desc d;
+        const uint32_t f = await_slot(sl, d);
         if (f == 0u) {
           more = false;
           break;
         }
         const uint32_t seg_end = min(r_end, s_end);
         if (f == kReadySample) {
-          Desc d;
-          ok = ok && desc_read(p.desc + static_cast<size_t>(sl) * kDescWords, d, err);
           const int c0 = static_cast<int>(it - sl * C2);
-          if (ok)
-            push(Claim{1, 0u, 0u, static_cast<int>(sl), c0,
-                       c0 + static_cast<int>(seg_end - it), {0, 0}, d});
+          push(Claim{1, 0u, 0u, static_cast<int>(sl), c0, c0 + static_cast<int>(seg_end - it),
+                     {0, 0}, d});
         } else {
           atomicMax(&p.hdr->b_next, s_end);  // an unused slot: pass it over
         }
