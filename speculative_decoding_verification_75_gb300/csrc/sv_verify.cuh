@@ -167,6 +167,14 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
   // The next step's kernel 0 may become resident beside this CTA; it waits
   // for this grid's completion before it touches the workspace.
   pdl_launch_dependents();
+  // The claimer's first row claim needs neither the staged tables nor the
+  // barrier: its round trips overlap them.
+  uint32_t n_row_items = 0, rb = 1, a_first = 0;
+  if (warp == kWarpClaimer && lane == 0) {
+    n_row_items = ld_cg(&p.hdr->n_rows) * static_cast<uint32_t>(p.C1);
+    rb = min(static_cast<uint32_t>(kRowBlock), max(1u, n_row_items / (2u * gridDim.x)));
+    a_first = atomicAdd(&p.hdr->a_next, rb);
+  }
   const bool smem_req = p.B <= kSmemReq;
   if (smem_req) {
     for (int i = threadIdx.x; i <= p.B; i += kThreads) row_start_s[i] = ld_cg(p.row_start + i);
@@ -292,12 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
     // ticket past the last reserved slot, once every request is merged, ends
     // the stream.  Row blocks are claimed one ahead, so the claim's round
     // trip overlaps the queueing of the block before.
-    const uint32_t n_row_items = ld_cg(&p.hdr->n_rows) * static_cast<uint32_t>(p.C1);
     const uint32_t C2 = static_cast<uint32_t>(p.C2);
-    // Claim sizes: up to kRowBlock / kResBlock items, fewer when the batch
-    // is small, so that its items spread over the grid.
+    // Claim sizes (rb: set above): up to kRowBlock / kResBlock items, fewer
+    // when the batch is small, so that its items spread over the grid.
     const uint32_t spread = 2u * gridDim.x;
-    const uint32_t rb = min(static_cast<uint32_t>(kRowBlock), max(1u, n_row_items / spread));
     const uint32_t rt = min(static_cast<uint32_t>(kResBlock),
                             max(1u, ld_cg(&p.hdr->n_valid) * C2 / spread));
     uint32_t k = 0;
@@ -325,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
         if (kPollNs) __nanosleep(kPollNs);
       }
     };
-    uint32_t a_cur = atomicAdd(&p.hdr->a_next, rb);
+    uint32_t a_cur = a_first;
     bool rows_left = true, more = true;
     while (ok && more) {
       if (rows_left) {
