@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -113,12 +114,20 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/CUDA source without comments or blank-line differences: an edit to
+    a comment leaves the compiled kernels, and so this hash, unchanged."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     src = ROOT / "speculative_decoding_verification_75_gb300" / "csrc"
     for f in sorted(src.glob("*")) + sorted((ROOT / "include").glob("*.h")):
         h.update(f.name.encode())
-        h.update(f.read_bytes())
+        h.update(_code_only(f.read_text()).encode())
     return h.hexdigest()[:16]
 
 

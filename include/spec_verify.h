@@ -23,6 +23,14 @@
  *   - Work is enqueued asynchronously on `stream` (NULL = legacy default
  *     stream).  Host-side argument checks return an error before anything is
  *     enqueued; a failed launch returns SV_ERR_CUDA.
+ *   - spec_verify and its variants launch their kernels as programmatic
+ *     dependent launches: their first kernel waits for the completion of
+ *     whatever precedes it on the stream before it touches memory, and the
+ *     last one allows the next kernel on the stream to be scheduled early.
+ *     A kernel launched after it WITH programmatic stream serialization must
+ *     wait for its prerequisites (griddepcontrol.wait /
+ *     cudaGridDependencySynchronize) before reading the outputs; ordinary
+ *     launches, copies and events are unaffected.
  *   - Invalid per-request DATA (a draft length outside [0, gamma_max], a
  *     temperature that is negative, NaN, inf or subnormal, a draft token id
  *     outside [0, V), a uniform outside [0, 1), a non-finite softmax
