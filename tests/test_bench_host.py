@@ -1,5 +1,6 @@
 """Host logic of bench.py on the CPU: arguments, seeds, the algorithmic
-byte count, the traffic record's source check, the reference arm's JSON
+byte count, the traffic record's source check (comment-insensitive), the
+reference arm's JSON
 line, and the multi-rank path (replicas sharded by request, timing taken as
 the maximum over ranks) on two gloo ranks."""
 import io
@@ -52,6 +53,23 @@ def test_recorded_traffic_needs_matching_sources(tmp_path, monkeypatch):
     f.write_text(json.dumps({"source_hash": "old", "dram_bytes_per_step": 123}))
     assert bench.recorded_traffic("c3") is None
     assert bench.recorded_traffic("c9") is None
+
+
+def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    csrc = tmp_path / "speculative_decoding_verification_75_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "include").mkdir()
+    monkeypatch.setattr(bench, "ROOT", tmp_path)
+    k = csrc / "k.cuh"
+    h = tmp_path / "include" / "a.h"
+    h.write_text("/* api */\nint f(int);\n")
+    k.write_text("// kernel\n__global__ void g(int *p) { p[0] = 1; }  // store\n")
+    base = bench.kernel_source_hash()
+    k.write_text("// kernel, reworded\n\n__global__ void g(int *p) { p[0] = 1; }\n")
+    h.write_text("/* api,\n   two lines */\nint f(int);  // f\n")
+    assert bench.kernel_source_hash() == base
+    k.write_text("__global__ void g(int *p) { p[0] = 2; }\n")
+    assert bench.kernel_source_hash() != base
 
 
 def test_reference_arm_prints_one_json_line():
