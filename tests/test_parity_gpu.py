@@ -98,6 +98,37 @@ def test_all_accepted_takes_bonus_row():
     assert (gpu["num_accepted"] == 4).all()
 
 
+# A batch of one request runs the kernel variant whose counter warp runs the
+# merge and the search itself; these cover its paths.
+@pytest.mark.parametrize("name,T,g,dtype,V,with_q", [
+    ("greedy", 0.0, 4, "bf16", 9000, True),
+    ("sampled_fp32", 1.0, 3, "fp32", 5000, True),
+    ("deterministic", 0.8, 5, "bf16", 12000, False),
+    ("gamma0", 1.0, 0, "bf16", 4000, True),
+    ("plain_load", 0.7, 3, "fp32", 4097, True),   # V * 4 not a multiple of 16
+])
+def test_single_request(name, T, g, dtype, V, with_q):
+    w = Workload("one_" + name, 1, g, V, dtype, 2.0, (0.5, 0.5), (T,), seed=21)
+    for seed in range(4):
+        case = make_case(w, device=DEV, seed=100 + seed, draft_probs=with_q)
+        check(case)
+
+
+def test_single_request_bonus_and_invalid():
+    w = Workload("one_bonus", 1, 4, 9000, "bf16", 2.0, (0.5, 0.5), (1.0,), seed=22)
+    case = make_case(w, device=DEV)
+    case["u_accept"].zero_()
+    case["draft_probs"] = torch.softmax(case["logits"][:, :4].float(), dim=-1).contiguous()
+    rep, gpu, _ = check(case)
+    assert int(gpu["num_accepted"][0]) == 4
+    case = make_case(w, device=DEV)
+    case["u_sample"][0] = float("nan")   # the merge marks it bad; no residual, no search
+    gpu = run_gpu(case)
+    ora = run_oracle(case)
+    compare(case, gpu, ora)
+    assert int(gpu["num_accepted"][0]) == -1
+
+
 def test_empty_residual_draws_from_p():
     w = Workload("empty", 8, 2, 3000, "fp32", 1.5, (0.5, 0.5), (1.0,), seed=12)
     case = make_case(w, device=DEV)
