@@ -76,18 +76,28 @@ class Oracle:
         lib.orc_verify.argtypes = [_P, ctypes.c_int, _P, _P, _P, _P, _P, _P,
                                    ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                    ctypes.POINTER(_Outputs)]
+        self.has_mt = hasattr(lib, "orc_verify_mt")
+        if self.has_mt:
+            lib.orc_verify_mt.restype = ctypes.c_int
+            lib.orc_verify_mt.argtypes = lib.orc_verify.argtypes + [ctypes.c_int]
         lib.orc_row_stats.restype = None
         lib.orc_row_stats.argtypes = [_P, ctypes.c_int, ctypes.c_size_t,
                                       ctypes.c_int, ctypes.c_double, _P, _P, _P]
+        lib.orc_draw_cdf.restype = ctypes.c_int
+        lib.orc_draw_cdf.argtypes = [_P, ctypes.c_int, _P, _P, _P, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
         lib.orc_inverse_cdf.restype = ctypes.c_int
         lib.orc_inverse_cdf.argtypes = [_P, ctypes.c_int, ctypes.c_double, _P]
         self.lib = lib
 
     def verify(self, logits, draft_ids, draft_probs, u_acc, u_samp,
-               temperature, draft_lens=None, *, is_bf16: Optional[bool] = None):
+               temperature, draft_lens=None, *, is_bf16: Optional[bool] = None,
+               nthreads: int = 1):
         """Run the oracle.  Shapes: logits [B, g+1, V] (uint16 bf16 bits or
         fp32), draft_ids [B, g], draft_probs [B, g, V] or None, u_acc [B, g],
-        u_samp [B], temperature [B], draft_lens [B] or None."""
+        u_samp [B], temperature [B], draft_lens [B] or None.  nthreads > 1
+        splits the requests over that many host threads (same arithmetic,
+        same results)."""
         if is_bf16 is None:
             logits, is_bf16 = logits_to_numpy(logits)
         else:
@@ -120,13 +130,32 @@ class Oracle:
             "row_argmax": np.empty((B, g + 1), np.int32),
         }
         outs = _Outputs(**{k: _ptr(v) for k, v in res.items()})
-        rc = self.lib.orc_verify(_ptr(logits), int(bool(is_bf16)),
-                                 _ptr(draft_ids), _ptr(draft_probs),
-                                 _ptr(u_acc), _ptr(u_samp), _ptr(temperature),
-                                 _ptr(draft_lens), B, g, V, ctypes.byref(outs))
+        args = [_ptr(logits), int(bool(is_bf16)), _ptr(draft_ids), _ptr(draft_probs),
+                _ptr(u_acc), _ptr(u_samp), _ptr(temperature), _ptr(draft_lens), B, g, V,
+                ctypes.byref(outs)]
+        if nthreads > 1 and self.has_mt:
+            rc = self.lib.orc_verify_mt(*args, int(nthreads))
+        else:
+            rc = self.lib.orc_verify(*args)
         if rc != 0:
             raise MemoryError("oracle scratch allocation failed")
         return res
+
+    def draw_cdf(self, logits, draft_ids, draft_probs, temperature, b: int, k: int, g: int):
+        """Inclusive prefix sums (fp64, [V]) of the weights of the draw at
+        position k of request b (g its draft length), as the oracle walks
+        them; None for a greedy request."""
+        arr, is_bf16 = logits_to_numpy(logits)
+        arr = np.ascontiguousarray(arr)
+        B, rows, V = arr.shape
+        gmax = rows - 1
+        ids = _c(_np(draft_ids).reshape(B, gmax), np.int32)
+        q = None if draft_probs is None else _c(_np(draft_probs).reshape(B, gmax, V), np.float32)
+        T = _c(_np(temperature).reshape(B), np.float32)
+        cdf = np.empty(V, np.float64)
+        rc = self.lib.orc_draw_cdf(_ptr(arr), int(bool(is_bf16)), _ptr(ids), _ptr(q), _ptr(T),
+                                   int(b), int(k), int(g), gmax, V, _ptr(cdf))
+        return None if rc != 0 else cdf
 
     def row_stats(self, row, temperature: float):
         """(max, normaliser, argmax) of the softmax of row / T for one row."""

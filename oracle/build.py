@@ -15,7 +15,7 @@ SRC = HERE / "oracle.c"
 LIB = HERE / "liboracle.so"
 
 CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-          "-fno-fast-math", "-Wall", "-Wextra"]
+          "-fno-fast-math", "-Wall", "-Wextra", "-pthread", "-D_POSIX_C_SOURCE=200809L"]
 
 
 def build_oracle(force: bool = False) -> Path:
@@ -24,7 +24,7 @@ def build_oracle(force: bool = False) -> Path:
             and LIB.stat().st_mtime >= SRC.stat().st_mtime):
         return LIB
     tmp = LIB.with_suffix(f".so.tmp{os.getpid()}")
-    cmd = ["gcc", *CFLAGS, str(SRC), "-o", str(tmp), "-lm"]
+    cmd = ["gcc", *CFLAGS, str(SRC), "-o", str(tmp), "-lm", "-pthread"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)
     return LIB

@@ -37,6 +37,7 @@
  * Everything is computed in fp64; bf16 and fp32 inputs convert to fp64 exactly.
  */
 #include <math.h>
+#include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -54,6 +55,11 @@ enum {
 
 /* P3 §5.2 step (2): the divisor of the acceptance ratio is clamped at 1e-10. */
 static const double ORC_Q_FLOOR = 1e-10;
+
+/* log2(e) and the largest finite binary32 value (the range check of the
+ * temperature-scaled row maximum). */
+static const double ORC_LOG2E = 1.4426950408889634;
+static const double ORC_FLT_MAX = 3.4028234663852886e38;
 
 /* Optional outputs.  Any pointer may be NULL except tokens / num_accepted.
  * Shapes: [B] per request, [B, gmax] per draft position, [B, gmax+1] per row.
@@ -206,11 +212,47 @@ static int request_bad_bits(const int32_t *draft_ids, const float *u_acc,
  *   draft_lens   [B]             int32 in [0, gmax], or NULL (all gmax)
  * Returns 0, or -1 if the scratch allocation fails.
  */
-int orc_verify(const void *logits, int is_bf16, const int32_t *draft_ids,
-               const float *draft_probs, const float *u_acc,
-               const float *u_samp, const float *temperature,
-               const int32_t *draft_lens, int B, int gmax, int V,
-               orc_outputs *out)
+/* The weights of the draw at position k of request b (P3 §3.1 step 4, §3.2,
+ * §5.2 (5)): r_j = (p_k(j) - q_k(j))_+ at a rejection (k < g), p_g(j) for the
+ * bonus draw (§5.3), written to r[0..V-1].  Returns S = sum_j (p_k - q_k)_+
+ * (the residual mass before the fallback) and sets *fallback when S = 0 made
+ * the draw use p_k itself. */
+static double draw_weights(const void *logits, int is_bf16, const int32_t *draft_ids,
+                           const float *draft_probs, int b, int k, int g, int gmax, int V,
+                           size_t off, double mx, double s, int argmax, double T,
+                           double *r, int *fallback)
+{
+    double S = 0.0;
+    for (int j = 0; j < V; ++j) {
+        double p = target_prob(logit_at(logits, is_bf16, off + (size_t)j), j, mx, s, argmax, T);
+        double q = 0.0; /* bonus row: nothing to subtract */
+        if (k < g) {
+            if (draft_probs)
+                q = (double)draft_probs[((size_t)b * gmax + k) * (size_t)V + j];
+            else
+                q = (j == draft_ids[(size_t)b * gmax + k]) ? 1.0 : 0.0;
+        }
+        r[j] = fmax(p - q, 0.0);
+        S += r[j];
+    }
+    *fallback = 0;
+    if (!(S > 0.0)) {
+        /* Reading: an empty residual means p_k <= q_k everywhere; draw from
+         * p_k itself. */
+        for (int j = 0; j < V; ++j)
+            r[j] = target_prob(logit_at(logits, is_bf16, off + (size_t)j), j, mx, s, argmax, T);
+        *fallback = 1;
+    }
+    return S;
+}
+
+/* Requests b0 .. b1-1 of the batch (each request is independent of the
+ * others; every output slot of a request is written by its own iteration). */
+static int verify_range(const void *logits, int is_bf16, const int32_t *draft_ids,
+                        const float *draft_probs, const float *u_acc,
+                        const float *u_samp, const float *temperature,
+                        const int32_t *draft_lens, int b0, int b1, int gmax, int V,
+                        orc_outputs *out)
 {
     const size_t rows_per_req = (size_t)gmax + 1;
     double *row_m = malloc(rows_per_req * sizeof(double));
@@ -222,7 +264,7 @@ int orc_verify(const void *logits, int is_bf16, const int32_t *draft_ids,
         return -1;
     }
 
-    for (int b = 0; b < B; ++b) {
+    for (int b = b0; b < b1; ++b) {
         int32_t *tok = out->tokens + (size_t)b * rows_per_req;
         for (size_t i = 0; i < rows_per_req; ++i)
             tok[i] = -1;
@@ -257,6 +299,13 @@ int orc_verify(const void *logits, int is_bf16, const int32_t *draft_ids,
                 orc_row_stats(logits, is_bf16, off, V, T, &row_m[i], &row_s[i],
                               &row_a[i]);
                 if (T > 0.0 && !(isfinite(row_m[i]) && isfinite(row_s[i])))
+                    bad |= ORC_BAD_NORMALISER;
+                /* Reading: the step works on binary32 logits (the pages' fp32
+                 * tensors), so a temperature so small that the row maximum
+                 * over T (in log2 units) leaves the binary32 range is invalid
+                 * data, like a non-finite normaliser. */
+                if (T > 0.0 && isfinite(row_m[i]) &&
+                    !(fabs(row_m[i]) * (ORC_LOG2E / T) < ORC_FLT_MAX))
                     bad |= ORC_BAD_NORMALISER;
             }
         }
@@ -312,29 +361,11 @@ int orc_verify(const void *logits, int is_bf16, const int32_t *draft_ids,
             tok[k] = row_a[k]; /* p_k is one-hot at its argmax */
             continue;
         }
-        double S = 0.0;
-        for (int j = 0; j < V; ++j) {
-            double p = target_prob(logit_at(logits, is_bf16, off + (size_t)j), j,
-                                   row_m[k], row_s[k], row_a[k], T);
-            double q = 0.0; /* bonus row: nothing to subtract */
-            if (k < g) {
-                if (draft_probs)
-                    q = (double)draft_probs[((size_t)b * gmax + k) * (size_t)V + j];
-                else
-                    q = (j == draft_ids[(size_t)b * gmax + k]) ? 1.0 : 0.0;
-            }
-            resid[j] = fmax(p - q, 0.0);
-            S += resid[j];
-        }
+        int fallback = 0;
+        double S = draw_weights(logits, is_bf16, draft_ids, draft_probs, b, k, g, gmax, V,
+                                off, row_m[k], row_s[k], row_a[k], T, resid, &fallback);
         if (out->resid_mass) out->resid_mass[b] = S;
-        if (!(S > 0.0)) {
-            /* Reading: an empty residual means p_k <= q_k everywhere; draw
-             * from p_k itself. */
-            for (int j = 0; j < V; ++j)
-                resid[j] = target_prob(logit_at(logits, is_bf16, off + (size_t)j),
-                                       j, row_m[k], row_s[k], row_a[k], T);
-            if (out->sample_fallback) out->sample_fallback[b] = 1;
-        }
+        if (out->sample_fallback) out->sample_fallback[b] = fallback;
         double margin = 0.0;
         tok[k] = orc_inverse_cdf(resid, V, (double)u_samp[b], &margin);
         if (out->sample_margin) out->sample_margin[b] = margin;
@@ -344,5 +375,108 @@ int orc_verify(const void *logits, int is_bf16, const int32_t *draft_ids,
     free(row_s);
     free(row_a);
     free(resid);
+    return 0;
+}
+
+int orc_verify(const void *logits, int is_bf16, const int32_t *draft_ids,
+               const float *draft_probs, const float *u_acc,
+               const float *u_samp, const float *temperature,
+               const int32_t *draft_lens, int B, int gmax, int V,
+               orc_outputs *out)
+{
+    return verify_range(logits, is_bf16, draft_ids, draft_probs, u_acc, u_samp,
+                        temperature, draft_lens, 0, B, gmax, V, out);
+}
+
+/* ---- the same step on several host threads (for timing on many cores) -- */
+
+typedef struct {
+    const void *logits;
+    int is_bf16;
+    const int32_t *draft_ids;
+    const float *draft_probs, *u_acc, *u_samp, *temperature;
+    const int32_t *draft_lens;
+    int b0, b1, gmax, V;
+    orc_outputs *out;
+    int rc;
+} orc_range_job;
+
+static void *run_range(void *arg)
+{
+    orc_range_job *j = (orc_range_job *)arg;
+    j->rc = verify_range(j->logits, j->is_bf16, j->draft_ids, j->draft_probs,
+                         j->u_acc, j->u_samp, j->temperature, j->draft_lens,
+                         j->b0, j->b1, j->gmax, j->V, j->out);
+    return NULL;
+}
+
+/* orc_verify with the requests split into contiguous ranges over nthreads
+ * POSIX threads.  The per-request arithmetic is verify_range's, unchanged;
+ * results are identical to orc_verify's.  Returns 0, or -1 if a scratch
+ * allocation or a thread creation fails. */
+int orc_verify_mt(const void *logits, int is_bf16, const int32_t *draft_ids,
+                  const float *draft_probs, const float *u_acc,
+                  const float *u_samp, const float *temperature,
+                  const int32_t *draft_lens, int B, int gmax, int V,
+                  orc_outputs *out, int nthreads)
+{
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > B) nthreads = B > 0 ? B : 1;
+    if (nthreads == 1)
+        return orc_verify(logits, is_bf16, draft_ids, draft_probs, u_acc, u_samp,
+                          temperature, draft_lens, B, gmax, V, out);
+    orc_range_job *jobs = calloc((size_t)nthreads, sizeof *jobs);
+    pthread_t *tid = calloc((size_t)nthreads, sizeof *tid);
+    int rc = 0;
+    if (!jobs || !tid) {
+        free(jobs); free(tid);
+        return -1;
+    }
+    int started = 0;
+    for (int k = 0; k < nthreads; ++k) {
+        orc_range_job *j = &jobs[k];
+        j->logits = logits; j->is_bf16 = is_bf16; j->draft_ids = draft_ids;
+        j->draft_probs = draft_probs; j->u_acc = u_acc; j->u_samp = u_samp;
+        j->temperature = temperature; j->draft_lens = draft_lens;
+        j->b0 = (int)((long long)B * k / nthreads);
+        j->b1 = (int)((long long)B * (k + 1) / nthreads);
+        j->gmax = gmax; j->V = V; j->out = out;
+        if (pthread_create(&tid[k], NULL, run_range, j) != 0) {
+            rc = -1;
+            break;
+        }
+        ++started;
+    }
+    for (int k = 0; k < started; ++k) {
+        pthread_join(tid[k], NULL);
+        if (jobs[k].rc != 0) rc = -1;
+    }
+    free(jobs);
+    free(tid);
+    return rc;
+}
+
+/* Test support: the inclusive prefix sums C_0 .. C_{V-1} of the weights the
+ * draw at position k of request b walks (draw_weights, with the request's
+ * row statistics recomputed), so that a drawn token j can be checked against
+ * its interval [C_{j-1}, C_j) when u * C_{V-1} falls near an edge.  Returns 0,
+ * or -1 for T <= 0 (no draw) or an allocation failure. */
+int orc_draw_cdf(const void *logits, int is_bf16, const int32_t *draft_ids,
+                 const float *draft_probs, const float *temperature, int b, int k, int g,
+                 int gmax, int V, double *cdf)
+{
+    const double T = (double)temperature[b];
+    if (!(T > 0.0)) return -1;
+    const size_t off = ((size_t)b * ((size_t)gmax + 1) + (size_t)k) * (size_t)V;
+    double mx, s;
+    int argmax, fallback;
+    orc_row_stats(logits, is_bf16, off, V, T, &mx, &s, &argmax);
+    draw_weights(logits, is_bf16, draft_ids, draft_probs, b, k, g, gmax, V, off, mx, s,
+                 argmax, T, cdf, &fallback);
+    double c = 0.0;
+    for (int j = 0; j < V; ++j) {
+        c += cdf[j];
+        cdf[j] = c;
+    }
     return 0;
 }

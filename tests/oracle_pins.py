@@ -18,6 +18,8 @@ the oracle disagrees with what the speculative-decoding tutorial page
   deterministic_drafts P3 §7 prompt lookup: q one-hot at the draft, lossless
   empty_residual       the reading for sum (p - q)_+ = 0: draw from p
   bad_inputs / ragged / zero_drafts  the documented edge-case contract
+  temperature_range    the reading that a temperature so small that the row
+                       maximum over T leaves the binary32 range is invalid
 
 ``scale`` shrinks the Monte Carlo sizes (the mutation tests use 0.1).
 """
@@ -361,8 +363,28 @@ def pin_zero_drafts(orc, scale=1.0):
     assert r["tokens"][0].tolist() == [1, -1]    # C = .5 .8 1; 0.6 -> 1
 
 
+def pin_temperature_range(orc, scale=1.0):
+    """Reading (the pages' logits are binary32 tensors): a request whose row
+    maximum over T, in log2 units, is not finite in binary32 has invalid
+    data (BAD_NORMALISER = 32), while the same tiny T with a row maximum of
+    0, or a small T that keeps the product finite, is a valid request."""
+    V = 4
+    T = np.array([1e-37, 1e-37, 1e-30], np.float32)
+    logits = np.zeros((3, 2, V), np.float32)
+    logits[0] = [[100.0, 1.0, 2.0, 3.0], [100.0, 1.0, 2.0, 3.0]]    # 100 * log2e / 1e-37 >> 3.4e38
+    logits[1] = [[0.0, -1.0, -2.0, -3.0], [0.0, -1.0, -2.0, -3.0]]  # maximum 0: offset 0
+    logits[2] = [[10.0, 1.0, 2.0, 3.0], [10.0, 1.0, 2.0, 3.0]]      # 1.4e31: finite
+    ids = np.zeros((3, 1), np.int32)
+    r = orc.verify(logits, ids, None, np.full((3, 1), 0.5, np.float32),
+                   np.full(3, 0.5, np.float32), T)
+    assert r["bad"].tolist() == [32, 0, 0]
+    assert r["num_accepted"][0] == -1
+    # the valid rows are one-hot at the maximum: draft 0 accepted, bonus 0
+    assert r["tokens"][1].tolist() == [0, 0] and r["tokens"][2].tolist() == [0, 0]
+
+
 ALL_PINS = [pin_worked_example, pin_lossless, pin_expected_emitted,
             pin_first_rejection, pin_clamp, pin_bonus, pin_greedy,
             pin_temperature, pin_normaliser, pin_inverse_cdf,
             pin_deterministic_drafts, pin_empty_residual, pin_bad_inputs,
-            pin_ragged, pin_zero_drafts]
+            pin_ragged, pin_zero_drafts, pin_temperature_range]

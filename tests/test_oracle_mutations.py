@@ -13,9 +13,9 @@ from oracle_pins import ALL_PINS
 MUTATIONS = {
     "ratio_transposed": ("P / fmax(q, ORC_Q_FLOOR)", "q / fmax(P, ORC_Q_FLOOR)", 1),
     "accept_not_strict": ("int f = u < a;", "int f = u <= a;", 1),
-    "residual_sign": ("resid[j] = fmax(p - q, 0.0);", "resid[j] = fmax(q - p, 0.0);", 1),
-    "residual_unclamped": ("resid[j] = fmax(p - q, 0.0);", "resid[j] = p - q;", 1),
-    "residual_is_q": ("resid[j] = fmax(p - q, 0.0);", "resid[j] = q;", 1),
+    "residual_sign": ("r[j] = fmax(p - q, 0.0);", "r[j] = fmax(q - p, 0.0);", 1),
+    "residual_unclamped": ("r[j] = fmax(p - q, 0.0);", "r[j] = p - q;", 1),
+    "residual_is_q": ("r[j] = fmax(p - q, 0.0);", "r[j] = q;", 1),
     "last_rejection": ("if (f == 0 && k == g)", "if (f == 0)", 1),
     "temperature_multiplies_stats": (
         "s += exp((logit_at(logits, is_bf16, row_offset + (size_t)j) - mx) / T);",
@@ -40,6 +40,7 @@ MUTATIONS = {
     "uniform_closed_interval": ("return u >= 0.0 && u < 1.0;", "return u >= 0.0 && u <= 1.0;", 1),
     "no_fallback": ("if (!(S > 0.0)) {", "if (0) {", 1),
     "greedy_ignored": ("if (T == 0.0)\n        return j == argmax ? 1.0 : 0.0;", "", 1),
+    "range_check_dropped": ("!(fabs(row_m[i]) * (ORC_LOG2E / T) < ORC_FLT_MAX)", "0", 1),
 }
 
 
@@ -49,7 +50,7 @@ def _build_mutant(tmp_path, name, old, new, count):
     msrc = tmp_path / f"{name}.c"
     msrc.write_text(src.replace(old, new))
     lib = tmp_path / f"lib{name}.so"
-    subprocess.run(["gcc", *CFLAGS, str(msrc), "-o", str(lib), "-lm"], check=True)
+    subprocess.run(["gcc", *CFLAGS, str(msrc), "-o", str(lib), "-lm", "-pthread"], check=True)
     return lib
 
 
