@@ -81,7 +81,9 @@ typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 #define SV_BAD_TOKEN 0x4u        /* a draft token id outside [0, V)         */
 #define SV_BAD_U_ACCEPT 0x8u     /* an acceptance uniform outside [0, 1)    */
 #define SV_BAD_U_SAMPLE 0x10u    /* the sampling uniform outside [0, 1)     */
-#define SV_BAD_NORMALISER 0x20u  /* non-finite softmax normaliser (T > 0)   */
+#define SV_BAD_NORMALISER 0x20u  /* non-finite softmax normaliser (T > 0),
+                                    or a row maximum whose value over T, in
+                                    log2 units, is not finite in binary32  */
 #define SV_FAULT_TIMEOUT 0x10000u/* a bounded wait inside a kernel gave up  */
 
 /*
@@ -257,8 +259,11 @@ SV_API const char *sv_status_string(sv_status status);
  *     before anything is enqueued (B=256, gamma_max=7, V=151936 needs about
  *     1 MiB).
  *   - The first call on a device looks up the scratch array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before capturing any stream on the device.
+ *     (cudaGetSymbolAddress, with that device current) and caches it for the
+ *     rest of the process; make that first call before capturing any stream
+ *     on the device.  The cached address does not survive a reset of the
+ *     device's primary context (cudaDeviceReset): calling this entry point
+ *     after such a reset is not supported.
  *   - Every call on a device shares the one array, and each call resets what
  *     must start at zero; calls whose work may overlap on the GPU (other
  *     streams, other host threads) race on it and must be serialised by the

@@ -306,8 +306,12 @@ __device__ __noinline__ void merge_request(const Params &p, int b, int nr, float
           s = __fadd_rn(s, __fmul_rn(bs, ex2(__fsub_rn(ob, offset(m, cs)))));
         }
       }
+      // A temperature so small that the row maximum over T (log2 units)
+      // leaves the binary32 range makes the offset, and so p, meaningless:
+      // invalid data, like a non-finite normaliser.
       if (greedy) s = 1.f;
-      else if (!(isfinite(m) && isfinite(s))) bad |= SV_BAD_NORMALISER;
+      else if (!(isfinite(m) && isfinite(s) && isfinite(offset(m, cs))))
+        bad |= SV_BAD_NORMALISER;
       if (dg.row_max) dg.row_max[static_cast<size_t>(b) * R + i] = m;
       // The normaliser as defined, sum exp2((l - m) * cs): the stored sum
       // times exp2(offset(m) - m * cs), whose exponent one fma forms exactly.

@@ -28,18 +28,22 @@ def check(case, **kw):
 
 @pytest.mark.parametrize("key", ["c1", "c2", "c3", "c4", "c5"])
 def test_workload_full_size(key):
+    """Every request of the workload: exact, or (draw near a CDF edge) exact
+    up to the draw and the draw within its bracket.  An accept decision
+    within 1e-5 of its uniform has probability ~2e-5 per decision, so at most
+    one such request is tolerated per workload; the counts are reported."""
     w = workloads.workload(key)
     case = make_case(w, device=DEV)
-    rep, gpu, ora = check(case)
-    print(f"\n{w.name}: {rep}")
-    assert rep["exact"] >= w.B // 4, rep
+    rep, gpu, ora = check(case, label=w.name)
+    assert rep["borderline"] <= 1, rep
+    assert rep["exact"] + rep["draw_border"] + rep["borderline"] + rep["bad"] == w.B
 
 
 @pytest.mark.parametrize("gamma", [3, 4, 5, 6, 7, 8])
 def test_gamma_sweep_c4_shape(gamma):
     w = workloads.workload("c4", B=16, gamma=gamma)
-    rep, _, _ = check(make_case(w, device=DEV))
-    assert rep["exact"] + rep["borderline"] == 16
+    rep, _, _ = check(make_case(w, device=DEV), label=f"c4 shape, B=16, gamma={gamma}")
+    assert rep["borderline"] <= 1 and rep["bad"] == 0
 
 
 SMALL_V = [1, 2, 7, 33, 1000, 1024, 4095, 4096, 4097, 8192, 8200, 20001, 20008]
@@ -178,6 +182,25 @@ def test_invalid_inputs_are_isolated():
     assert word == 1 | 2 | 4 | 8 | 16 | 32
 
 
+def test_tiny_temperature_is_invalid_data():
+    """A temperature so small that the row maximum over T leaves the binary32
+    range marks the request bad (SV_BAD_NORMALISER), as the oracle does; the
+    same temperature with a row maximum of 0 is a valid (one-hot) request."""
+    B, g, V = 4, 2, 4096
+    w = Workload("tinyT", B, g, V, "fp32", 1.0, (0.5, 0.5), (1.0,), seed=17)
+    case = make_case(w, device=DEV)
+    lg = case["logits"]
+    lg[0, :, :] = torch.linspace(-3.0, 100.0, V, device=DEV)   # 100 * log2e / 1e-37 overflows
+    lg[1, :, :] = torch.linspace(-3.0, 0.0, V, device=DEV)     # maximum 0: offset 0
+    case["temperature"][0] = 1e-37
+    case["temperature"][1] = 1e-37
+    gpu = run_gpu(case)
+    ora = run_oracle(case)
+    compare(case, gpu, ora)
+    assert ora["bad"].tolist()[:2] == [32, 0]
+    assert int(gpu["num_accepted"][0]) == -1 and int(gpu["num_accepted"][1]) >= 0
+
+
 def test_no_request_with_rows_ends_cleanly():
     """Every draft length out of range: nothing is streamed or merged; the
     call still ends without a timeout and marks every request."""
@@ -214,7 +237,7 @@ def test_bounded_waits_give_up_and_leave_the_context_usable():
     assert word == api.SV_FAULT_TIMEOUT | 0x1 | 0x2, hex(word)
     case = make_case(workloads.workload("c1"), device=DEV)
     rep, _, _ = check(case)
-    assert rep["exact"] + rep["borderline"] == 1
+    assert rep["exact"] + rep["draw_border"] + rep["borderline"] == 1
 
 
 def test_clean_call_reports_ok():
@@ -232,6 +255,48 @@ def test_deterministic_and_stream():
         b = run_gpu(case)
     for k in a:
         assert np.array_equal(a[k], b[k], equal_nan=True), k
+
+
+def test_two_streams_run_concurrently_with_their_own_workspaces():
+    """verify() on two streams at once: each stream gets its own cached
+    workspace, so the calls may overlap on the GPU; both match the oracle."""
+    cases = [make_case(workloads.workload("c2"), device=DEV, seed=s) for s in (31, 32)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    outs = []
+    for _ in range(3):  # several rounds so the two streams' calls overlap
+        outs = []
+        for c, s in zip(cases, streams):
+            with torch.cuda.stream(s):
+                outs.append(verify(c["logits"], c["draft_ids"], c["draft_probs"],
+                                   c["u_accept"], c["u_sample"], c["temperature"],
+                                   c["draft_lens"], diag=True, stream=s))
+    torch.cuda.synchronize()
+    ws = [api.get_workspace(8, 5, 151936, DEV, s) for s in streams]
+    assert ws[0].data_ptr() != ws[1].data_ptr()
+    for c, (tok, nacc, d) in zip(cases, outs):
+        gpu = {"tokens": to_np(tok), "num_accepted": to_np(nacc)}
+        gpu.update({k: to_np(v) for k, v in d.items()})
+        compare(c, gpu, run_oracle(c))
+
+
+def test_bound_call_matches_verify():
+    """bind(): the arguments are marshalled once; repeated calls give
+    verify()'s results and follow the tensors' current contents."""
+    c = make_case(workloads.workload("c2"), device=DEV, seed=33)
+    args = (c["logits"], c["draft_ids"], c["draft_probs"], c["u_accept"], c["u_sample"],
+            c["temperature"], c["draft_lens"])
+    ref_tok, ref_nacc = verify(*args)
+    bound = api.bind(*args)
+    for _ in range(3):
+        tok, nacc = bound()
+    torch.cuda.synchronize()
+    assert torch.equal(tok, ref_tok) and torch.equal(nacc, ref_nacc)
+    c["u_sample"].copy_(torch.rand_like(c["u_sample"]))   # new contents, same storage
+    tok, nacc = bound()
+    ref_tok, ref_nacc = verify(*args)
+    torch.cuda.synchronize()
+    assert torch.equal(tok, ref_tok) and torch.equal(nacc, ref_nacc)
 
 
 def test_batch_zero_is_noop():
