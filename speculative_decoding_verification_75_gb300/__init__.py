@@ -2,7 +2,8 @@
 
 ``verify`` runs one verification step of a batch on the GPU through the C ABI
 of ``lib/libspecverify.so`` (declared in ``include/spec_verify.h``);
+``bind`` fixes the tensors of a loop once and re-runs the step cheaply;
 ``verify_host`` does the same from host tensors, copies included.
 """
-from .api import (SpecVerifyError, last_error, load_library, verify,  # noqa: F401
-                  verify_host, workspace_bytes)
+from .api import (BoundVerify, SpecVerifyError, bind, last_error,  # noqa: F401
+                  load_library, verify, verify_host, workspace_bytes)
