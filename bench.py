@@ -50,7 +50,11 @@ def parse_args(argv=None):
     ap.add_argument("--sets", type=int, default=0,
                     help="rotating input sets (0: enough to exceed 3x L2)")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=20.0,
+                    help="wall time of the CPU baseline (half single-thread, half all cores)")
+    ap.add_argument("--sweep-steps", type=int, default=200,
+                    help="calls timed per workload of the B x gamma x V sweep")
+    ap.add_argument("--no-sweep", action="store_true")
     return ap.parse_args(argv)
 
 
@@ -194,56 +198,90 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- our arm ----
 
+def make_sets(W, w, dev, rank, min_bytes, max_sets):
+    """Rotating input sets of workload ``w`` until they exceed ``min_bytes``
+    (at least two, at most ``max_sets``).  Returns (cases, bytes per set)."""
+    cases, set_bytes = [], 0
+    while True:
+        c = W.make_case(w, device=dev, seed=rank_seed(w.seed, rank, len(cases)))
+        cases.append(c)
+        set_bytes = sum(t.numel() * t.element_size() for t in c.values() if t is not None)
+        if len(cases) >= max_sets or (len(cases) >= 2 and len(cases) * set_bytes >= min_bytes):
+            return cases, set_bytes
+
+
+def step_bytes(case, nacc, V):
+    """Algorithmic bytes of one call on ``case`` given its num_accepted."""
+    w_g = case["draft_ids"].shape[1]
+    lens = (case["draft_lens"].cpu().tolist() if case["draft_lens"] is not None
+            else [w_g] * case["draft_ids"].shape[0])
+    return algorithmic_bytes(lens, case["temperature"].cpu().tolist(), nacc.cpu().tolist(), V,
+                             case["logits"].element_size(), case["draft_probs"] is not None)
+
+
+def time_workload(api, W, w, dev, steps, warmup, flush_buf=None):
+    """Device time of one call of workload ``w``: rotating input sets larger
+    than L2 timed back to back, or (sets too small to defeat L2) each call
+    timed on its own with an L2 flush between calls.  Returns a dict."""
+    import torch
+    cases, set_bytes = make_sets(W, w, dev, 0, 3 * L2_BYTES, 32)
+    rotate = len(cases) * set_bytes >= 3 * L2_BYTES
+    bound = [api.bind(c["logits"], c["draft_ids"], c["draft_probs"], c["u_accept"],
+                      c["u_sample"], c["temperature"], c["draft_lens"]) for c in cases]
+    n = len(bound)
+    for i in range(max(warmup, 3)):
+        bound[i % n]()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    if rotate:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            bound[i % n]()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) * 1e3 / steps
+        how = f"{n} rotating input sets of {set_bytes / 1e6:.1f} MB, back to back"
+    else:
+        times = []
+        for i in range(steps):
+            flush_buf.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            bound[i % n]()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(e0.elapsed_time(e1) * 1e3)
+        us = statistics.median(times)
+        how = (f"median of {steps} single calls, L2 flushed ({flush_buf.numel() / 1e6:.0f} MB "
+               f"written) before each")
+    by = sum(step_bytes(c, b.out_num_accepted, w.V) for c, b in zip(cases, bound)) / n
+    nacc = torch.cat([b.out_num_accepted for b in bound]).float()
+    rows = W.verified_rows(cases[0])
+    return {"us_per_step": us, "rows_per_s": rows / (us * 1e-6), "bytes_per_step": by,
+            "alpha_hat": float(nacc[nacc >= 0].mean()) / max(w.gamma, 1), "timing": how}
+
+
 def run_ours(args, rank, local_rank, world):
     import torch
 
-    from speculative_decoding_verification_75_gb300 import api, verify, verify_host
+    from speculative_decoding_verification_75_gb300 import api, verify_host
     from speculative_decoding_verification_75_gb300 import workloads as W
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     api.load_library()
     w = W.workload(args.workload)
-    set_bytes = None
-    cases = []
-    nsets = args.sets
-    while True:
-        c = W.make_case(w, device=dev, seed=rank_seed(w.seed, rank, len(cases)))
-        cases.append(c)
-        set_bytes = sum(t.numel() * t.element_size() for t in c.values() if t is not None)
-        if nsets and len(cases) >= nsets:
-            break
-        if not nsets and (len(cases) * set_bytes >= 3 * L2_BYTES and len(cases) >= 2):
-            break
+    cases, set_bytes = make_sets(W, w, dev, rank, 3 * L2_BYTES if not args.sets else 0,
+                                 args.sets or 64)
     nsets = len(cases)
     rows_per_step = W.verified_rows(cases[0])
-    outs = [(torch.empty(w.B, w.gamma + 1, dtype=torch.int32, device=dev),
-             torch.empty(w.B, dtype=torch.int32, device=dev)) for _ in cases]
-    ws = api.get_workspace(w.B, w.gamma, w.V, dev)
-
-    def step(i):
-        c = cases[i % nsets]
-        o = outs[i % nsets]
-        verify(c["logits"], c["draft_ids"], c["draft_probs"], c["u_accept"],
-               c["u_sample"], c["temperature"], c["draft_lens"],
-               out_tokens=o[0], out_num_accepted=o[1], workspace=ws)
-
-    for i in range(max(args.warmup, 3)):
-        step(i)
-    torch.cuda.synchronize(dev)
-
-    # Algorithmic bytes of each input set (depend on where requests reject).
-    logit_bytes = cases[0]["logits"].element_size()
-    per_set_bytes = []
-    for c, o in zip(cases, outs):
-        lens = (c["draft_lens"].cpu().tolist() if c["draft_lens"] is not None
-                else [w.gamma] * w.B)
-        per_set_bytes.append(algorithmic_bytes(
-            lens, c["temperature"].cpu().tolist(), o[1].cpu().tolist(), w.V,
-            logit_bytes, c["draft_probs"] is not None))
-    mean_bytes = sum(per_set_bytes[i % nsets] for i in range(args.steps)) / args.steps
-    acc = torch.cat([o[1] for o in outs]).float()
-    alpha_hat = float(acc.mean()) / w.gamma
+    # The tensors of each set are bound once: a timed call is the C-ABI call
+    # with marshalled arguments (host cost ~5 us, far below the step).
+    bound = [api.bind(c["logits"], c["draft_ids"], c["draft_probs"], c["u_accept"],
+                      c["u_sample"], c["temperature"], c["draft_lens"]) for c in cases]
 
     barrier = (lambda: __import__("torch.distributed").distributed.barrier()) if world > 1 \
         else (lambda: None)
@@ -252,11 +290,14 @@ def run_ours(args, rank, local_rank, world):
     stream = torch.cuda.current_stream(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    # Warm-up directly before the timed region (no host work in between).
+    for i in range(max(args.warmup, 3)):
+        bound[i % nsets]()
     barrier()
     torch.cuda.synchronize(dev)
     e0.record(stream)
     for i in range(args.steps):
-        step(i)
+        bound[i % nsets]()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -267,11 +308,20 @@ def run_ours(args, rank, local_rank, world):
     rows_all = aggregate_sum(float(rows_per_step), world)
     value = rows_all / (ms_step / 1e3)
 
+    # Algorithmic bytes of each input set (they depend on where requests
+    # reject; the outputs of the timed calls are those of the warm-up).
+    per_set_bytes = [step_bytes(c, b.out_num_accepted, w.V) for c, b in zip(cases, bound)]
+    mean_bytes = sum(per_set_bytes[i % nsets] for i in range(args.steps)) / args.steps
+    acc = torch.cat([b.out_num_accepted for b in bound]).float()
+    alpha_hat = float(acc.mean()) / w.gamma
+
     # End to end through the public API from pinned host buffers: each step
     # copies its inputs to the device and reads its outputs back.
     host = []
     for c in cases[:2]:
         host.append({k: (None if v is None else v.cpu().pin_memory()) for k, v in c.items()})
+    del bound, cases
+    torch.cuda.empty_cache()
     h2d = sum(t.numel() * t.element_size() for t in host[0].values() if t is not None)
     d2h = w.B * (w.gamma + 1) * 4 + w.B * 4
     for i in range(2):
@@ -305,7 +355,10 @@ def run_ours(args, rank, local_rank, world):
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
                    "reasons": clk["reasons"], "samples": clk["samples"]},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
+                "h2d_gbs": h2d / e2e_s / 1e9,
+                "path": "verify_host: pinned host tensors copied to the device, one call, "
+                        "outputs copied back, every step"},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "roofline": {"bound": "hbm", "kernel": "spec_verify step (prepare + persistent sv_verify_kernel)",
                      "achieved": achieved, "peak": peak,
@@ -314,30 +367,69 @@ def run_ours(args, rank, local_rank, world):
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s"},
     }
+    if rank == 0 and world == 1 and not args.no_sweep:
+        line["sweep"] = sweep(api, W, dev, args, peak)
     if rank == 0 and world == 1:
-        line["cpu_baseline"] = cpu_baseline(cases[0], args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(host[0], args.cpu_seconds)
     return line
 
 
-def cpu_baseline(case, seconds: float):
+SWEEP = [("c1", {}), ("c2", {}), ("c3", {}), ("c4", {}), ("c5", {})] + \
+    [(f"c4_gamma{g}", {"gamma": g}) for g in range(3, 9)]
+
+
+def sweep(api, W, dev, args, peak):
+    """The B x gamma x V sweep: every workload (and c4's gamma 3..8 on the
+    same seed), each timed on its own inputs.  Throughput in verified draft
+    rows/s and algorithmic GB/s with its fraction of the measured HBM rate;
+    c1 moves ~1 MB, so its figure of merit is the latency of one call."""
+    import torch
+    flush = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
+    out = {}
+    for key, over in SWEEP:
+        w = W.workload(key.split("_")[0], **over)
+        r = time_workload(api, W, w, dev, args.sweep_steps, 3, flush)
+        gbs = r["bytes_per_step"] / (r["us_per_step"] * 1e-6) / 1e9
+        out[key] = {"workload": w.name if not over else f"{w.name} (gamma={w.gamma})",
+                    "B": w.B, "gamma": w.gamma, "V": w.V, "dtype": w.dtype,
+                    "us_per_step": r["us_per_step"], "rows_per_s": r["rows_per_s"],
+                    "gbs": gbs, "frac": gbs / peak, "alpha_hat": r["alpha_hat"],
+                    "timing": r["timing"]}
+        if key == "c1":
+            out[key]["figure_of_merit"] = "latency (us per call)"
+        torch.cuda.empty_cache()
+    return out
+
+
+def cpu_baseline(host, seconds: float):
     """The fp64 oracle, as it stands, on the host cores: whole batches of the
-    workload repeated until ``seconds`` of CPU time have passed."""
+    workload repeated until ``seconds`` of wall time have passed, once on one
+    thread and once split by request over every core this process may use."""
     import oracle
-    host = {k: (None if v is None else v.cpu()) for k, v in case.items()}
     rows = host["draft_ids"].shape[0] * host["draft_ids"].shape[1] \
         if host["draft_lens"] is None else int(host["draft_lens"].sum())
-    n, t0 = 0, time.perf_counter()
-    while True:
-        oracle.verify(host["logits"], host["draft_ids"], host["draft_probs"],
-                      host["u_accept"], host["u_sample"], host["temperature"],
-                      host["draft_lens"])
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return {"value": n * rows / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} full batch(es) of {host['draft_ids'].shape[0]} requests, "
-                      f"single-threaded fp64 C oracle, {el:.1f} s"}
+    args = (host["logits"], host["draft_ids"], host["draft_probs"], host["u_accept"],
+            host["u_sample"], host["temperature"], host["draft_lens"])
+
+    def timed(nthreads, budget):
+        n, t0 = 0, time.perf_counter()
+        while True:
+            oracle.verify(*args, nthreads=nthreads)
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= budget:
+                return n, el
+
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    n1, el1 = timed(1, seconds / 2)
+    nn, eln = timed(cores, seconds / 2)
+    B = host["draft_ids"].shape[0]
+    return {"value": nn * rows / eln, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{nn} full batch(es) of {B} requests, fp64 C oracle split by request "
+                      f"over {cores} threads, {eln:.1f} s",
+            "single_thread": {"value": n1 * rows / el1, "unit": UNIT, "cores": 1,
+                              "sample": f"{n1} full batch(es) of {B} requests, one thread, "
+                                        f"{el1:.1f} s"}}
 
 
 # ---------------------------------------------------------- reference arm ----
