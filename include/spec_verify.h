@@ -90,7 +90,10 @@ typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
  * Workspace size in bytes for a batch of B requests with up to gamma_max
  * drafts each over a V-token vocabulary (any logits dtype).  The workspace
  * must be device memory aligned to 256 bytes.  It needs no initialisation:
- * every call resets the parts it reads.  Returns 0 for invalid sizes.
+ * each call leaves it ready for the next (its work counters alternate
+ * between two sets by call), and a call that finds it not ready -- fresh or
+ * foreign bytes, another (B, gamma_max, V), a call that gave up -- clears it
+ * first.  Returns 0 for invalid sizes.
  */
 SV_API size_t sv_workspace_bytes(int B, int gamma_max, int V);
 
@@ -264,8 +267,8 @@ SV_API const char *sv_status_string(sv_status status);
  *     on the device.  The cached address does not survive a reset of the
  *     device's primary context (cudaDeviceReset): calling this entry point
  *     after such a reset is not supported.
- *   - Every call on a device shares the one array, and each call resets what
- *     must start at zero; calls whose work may overlap on the GPU (other
+ *   - Every call on a device shares the one array, which each call leaves
+ *     ready for the next; calls whose work may overlap on the GPU (other
  *     streams, other host threads) race on it and must be serialised by the
  *     caller, e.g. by issuing them on one stream.
  *   - Invalid per-request data is reported through out_num_accepted = -1

@@ -1,17 +1,20 @@
 // spec_verify.cu -- C ABI of the GB300 speculative-decoding verification
-// library: argument checks, workspace carving and the two launches.
+// library: argument checks, workspace carving and the launches.
 //
-//   kernel 0  sv_prepare_kernel  per-request row offsets and softmax scales,
-//                                reset of the per-call counters, rejection of
-//                                bad draft lengths
+//   kernel 0  sv_prepare_kernel  only for batches of more than kSmemReq
+//                                requests (row offsets and softmax scales in
+//                                global memory) or when the caller asks for
+//                                the acceptance histogram (its reset)
 //   kernel 1  sv_verify_kernel   persistent: softmax statistics of every row,
 //                                accept test and first rejection per request,
 //                                residual / bonus draw for sampled requests
 //
-// Kernel 1 is launched with programmatic stream serialisation so that its
-// launch and prologue overlap kernel 0.  It comes in a TMA variant (rows
-// start on 16-byte boundaries) and a plain-load variant for any other
-// alignment.
+// Both are launched with programmatic stream serialisation, so that a
+// launch and its prologue overlap the end of the grid before it.  Kernel 1
+// comes in a TMA variant (rows start on 16-byte boundaries) and a plain-load
+// variant for any other alignment.  It keeps the workspace ready for the
+// next call itself (counter sets alternate by call, see sv_layout.cuh), so
+// a call is one launch.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -104,7 +107,9 @@ sv_status launch_all(Params &p, cudaStream_t st, int dev, int nsm) {
   if (ensure_smem(kv, smem, local ? smem_done_local : smem_done, dev) != cudaSuccess)
     return SV_ERR_CUDA;
 
-  if (launch_pdl(sv_prepare_kernel, dim3(1), dim3(kPrepThreads), 0, st, p) != cudaSuccess)
+  p.tables_global = p.B > kSmemReq ? 1 : 0;
+  if ((p.tables_global || p.diag.accept_hist) &&
+      launch_pdl(sv_prepare_kernel, dim3(1), dim3(kPrepThreads), 0, st, p) != cudaSuccess)
     return SV_ERR_CUDA;
 
   const long long max_items = static_cast<long long>(p.B) * (p.gmax + 1) * p.C1;
@@ -209,13 +214,14 @@ sv_status spec_verify_diag(const void *target_logits, sv_dtype logits_dtype,
 
 sv_status sv_last_error(const void *workspace, sv_stream_t stream, uint32_t *out_word) {
   if (!workspace) return SV_ERR_INVALID_ARG;
-  uint32_t word = 0;
+  // The header's first words: the epoch (calls completed) and the error
+  // words of the two call parities; the last call ran with epoch - 1.
+  uint32_t head[3] = {0, 0, 0};
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const auto *hdr = static_cast<const sv::Header *>(workspace);
-  if (cudaMemcpyAsync(&word, &hdr->err, sizeof word, cudaMemcpyDeviceToHost, st) !=
-          cudaSuccess ||
+  if (cudaMemcpyAsync(head, workspace, sizeof head, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
       cudaStreamSynchronize(st) != cudaSuccess)
     return SV_ERR_CUDA;
+  const uint32_t word = head[1 + ((head[0] - 1u) & 1u)];
   if (out_word) *out_word = word;
   if (word & SV_FAULT_TIMEOUT) return SV_ERR_TIMEOUT;
   if (word) return SV_ERR_BAD_INPUT_DATA;

@@ -286,6 +286,14 @@ __device__ __forceinline__ uint64_t ld_relaxed64(const uint64_t *p) {
   asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ void st_release64(uint64_t *p, uint64_t v) {
+  asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_acquire64(const uint64_t *p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
 // Two adjacent 32-bit counters read in one access (8-byte aligned).
 __device__ __forceinline__ uint2 ld_relaxed2(const uint32_t *p) {
   uint2 v;

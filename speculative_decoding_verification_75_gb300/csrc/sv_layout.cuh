@@ -39,30 +39,83 @@ constexpr int kMinResChunk = kStageBytes / 8 / kSeg * kSeg;  // fp32 logits + q
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kQFloor = 1e-10f;  // clamp of the acceptance divisor
 
-struct __align__(128) Header {  // 512 bytes: four 128-byte lines
-  uint32_t err;       // SV_BAD_* | SV_FAULT_* bits of this call
-  uint32_t n_rows;    // active rows over all requests
-  uint32_t n_valid;   // requests with rows (each is merged once)
-  uint32_t a_next;    // next row-statistics item to hand out
-  uint32_t pad0[28];  // the residual queue sits on its own 128-byte line
+// Work counters of one call.  Consecutive calls on a workspace alternate
+// between two sets: a call runs on set (epoch & 1) while its CTA 0 clears
+// set (epoch + 1) & 1 for the next call, so no call has to reset state that
+// its own CTAs are about to use.
+struct __align__(128) Counters {  // 512 bytes: four 128-byte lines
+  uint32_t a_next;      // row-statistics items handed out after the static first blocks
+  uint32_t pad0[31];
   uint32_t b_next;      // next residual item to hand out: chunk c of the
                         // descriptor in slot s is item s * C2 + c
   uint32_t b_reserved;  // descriptor slots reserved (read with b_next)
-  uint32_t n_merged;    // requests merged so far
+  uint32_t n_merged;    // requests finished (merged, or rejected for their length)
   uint32_t pad1[29];
-  uint32_t jq_head;   // job tickets handed out
-  uint32_t pad2[31];
+  uint32_t jq_head;     // job tickets handed out
+  uint32_t exited;      // CTAs that have finished
+  uint32_t pad2[30];
   uint32_t all_merged;  // set by the last merge: b_reserved is final
   uint32_t pad3[31];    // (a line that is only read until then)
 };
 
-// jflag[j]: job j not (yet) due / due / never due.  Job b < B merges request
-// b; job B + s searches the residual of descriptor slot s.
-constexpr uint32_t kJobWait = 0u, kJobDue = 1u, kJobNone = 2u;
+struct __align__(128) Header {
+  uint32_t epoch;     // calls completed on this workspace (advanced by the last CTA out)
+  uint32_t err[2];    // SV_BAD_* | SV_FAULT_* bits of the call with that epoch parity
+  uint32_t pad0;
+  uint64_t ready[2];  // certificate that counter set s is clear for the call it serves
+  uint64_t pad1[13];
+  Counters set[2];
+};
 
-// State of descriptor slot s: reserved but not yet written / holds a row to
-// re-sample / holds nothing (its request turned out invalid).
+static_assert(offsetof(Header, epoch) == 0 && offsetof(Header, err) == 4,
+              "sv_last_error reads the epoch and both error words as three words");
+static_assert(offsetof(Header, ready) % 8 == 0 && offsetof(Header, set) % 128 == 0 &&
+                  offsetof(Counters, b_reserved) == offsetof(Counters, b_next) + 4,
+              "header alignment");
+
+// Certificate of counter set (e & 1) for the call with epoch e on a workspace
+// laid out for (B, gmax, V): any other value in ready[] -- a fresh or
+// foreign workspace, another layout, a call that faulted -- makes the call
+// clear the set itself before using it.
+__host__ __device__ inline uint64_t mix64(uint64_t x) {
+  x ^= x >> 30;
+  x *= 0xbf58476d1ce4e5b9ull;
+  x ^= x >> 27;
+  x *= 0x94d049bb133111ebull;
+  return x ^ (x >> 31);
+}
+__host__ __device__ inline uint64_t certificate(int B, int gmax, int V, uint32_t e) {
+  uint64_t x = mix64(0x7376636572746966ull ^ (static_cast<uint64_t>(static_cast<uint32_t>(B)) << 32) ^
+                     static_cast<uint32_t>(V));
+  x = mix64(x ^ (static_cast<uint64_t>(static_cast<uint32_t>(gmax)) << 32) ^ e);
+  return x | 1ull;
+}
+
+// Job flags and descriptor states carry the call's epoch: a value is current
+// only if its tag matches, so neither array is ever reset between calls.
+constexpr uint32_t kEpochMask = 0x3fffffffu;
+__device__ __forceinline__ uint32_t epoch_tag(uint32_t e) { return (e & kEpochMask) << 2; }
+
+// jflag[j] (with the call's tag): job j due / never due; any other value:
+// not (yet) due.  Job b < B merges request b; job B + s searches the
+// residual of descriptor slot s.
+constexpr uint32_t kJobDue = 1u, kJobNone = 2u;
+
+// State of descriptor slot s (with the call's tag): holds a row to
+// re-sample / holds nothing (its request turned out invalid); any other
+// value: reserved but not yet written.
 constexpr uint32_t kPending = 0u, kReadySample = 1u, kReadySkip = 2u;
+
+// What a CTA knows of its call once the workspace header is checked.
+struct Ctl {
+  Counters *ctr;  // this call's counter set
+  uint32_t *k1;   // [B] row-statistics chunks completed, this call's set
+  uint32_t *k2;   // [B] residual chunks completed, this call's set
+  uint32_t *err;  // this call's error word
+  uint32_t tag;   // epoch_tag(epoch)
+  uint32_t epoch;
+  uint32_t ok;    // 0: the set could not be made clear (a fault); do no work
+};
 
 struct __align__(8) Part {  // per (row, chunk) partial statistics
   float m;                  // chunk maximum logit
@@ -83,7 +136,7 @@ struct __align__(16) Desc {
 static_assert(sizeof(Desc) == 32, "eight 32-bit fields");
 
 // A descriptor slot holds the eight fields of a Desc in eight 64-bit words,
-// field i in the low half of word i and the slot's state in the high half.
+// field i in the low half of word i and the slot's tagged state in the high half.
 // The merge writes the words with relaxed 64-bit stores (each single-copy
 // atomic) and no fence; a reader takes the slot once every word carries the
 // state: a word can only show the state together with its own field, so no
@@ -100,26 +153,28 @@ __device__ __forceinline__ void desc_publish(uint64_t *w, const Desc &d, uint32_
 
 
 // One poll of a slot: all eight words in one round trip.  kReadySample only
-// once every word carries it (d is then complete), kReadySkip as word 0
-// shows it, else kPending.
-__device__ __forceinline__ uint32_t desc_poll(const uint64_t *w, Desc &d) {
+// once every word carries it with the call's tag (d is then complete),
+// kReadySkip as word 0 shows it, else kPending.
+__device__ __forceinline__ uint32_t desc_poll(const uint64_t *w, Desc &d, uint32_t tag) {
   uint32_t *f = reinterpret_cast<uint32_t *>(&d);
   uint64_t v[kDescWords];
 #pragma unroll
   for (int i = 0; i < kDescWords; ++i) v[i] = ld_relaxed64(w + i);
   const uint32_t s0 = static_cast<uint32_t>(v[0] >> 32);
-  if (s0 != kReadySample) return s0;
+  if (s0 == (tag | kReadySkip)) return kReadySkip;
+  if (s0 != (tag | kReadySample)) return kPending;
   bool all = true;
 #pragma unroll
   for (int i = 0; i < kDescWords; ++i) {
-    all = all && static_cast<uint32_t>(v[i] >> 32) == kReadySample;
+    all = all && static_cast<uint32_t>(v[i] >> 32) == (tag | kReadySample);
     f[i] = static_cast<uint32_t>(v[i]);
   }
   return all ? kReadySample : kPending;
 }
 
 // Waits (bounded) until every word of a kReadySample slot has landed.
-__device__ __forceinline__ bool desc_read(const uint64_t *w, Desc &d, uint32_t *err) {
+__device__ __forceinline__ bool desc_read(const uint64_t *w, Desc &d, uint32_t tag,
+                                          uint32_t *err) {
   uint32_t *f = reinterpret_cast<uint32_t *>(&d);
   const uint64_t t0 = global_timer_ns();
   for (;;) {
@@ -129,7 +184,7 @@ __device__ __forceinline__ bool desc_read(const uint64_t *w, Desc &d, uint32_t *
     bool all = true;
 #pragma unroll
     for (int i = 0; i < kDescWords; ++i) {
-      all = all && static_cast<uint32_t>(v[i] >> 32) == kReadySample;
+      all = all && static_cast<uint32_t>(v[i] >> 32) == (tag | kReadySample);
       f[i] = static_cast<uint32_t>(v[i]);
     }
     if (all) return true;
@@ -174,8 +229,8 @@ inline Layout make_layout(int B, int gmax, int V) {
   L.hdr = take(sizeof(Header));
   L.row_start = take(sizeof(int) * (static_cast<size_t>(B) + 1));
   L.cs = take(sizeof(float) * B);
-  L.k1_cnt = take(sizeof(uint32_t) * B);
-  L.k2_cnt = take(sizeof(uint32_t) * B);
+  L.k1_cnt = take(sizeof(uint32_t) * 2 * B);  // one array per counter set
+  L.k2_cnt = take(sizeof(uint32_t) * 2 * B);
   L.desc = take(sizeof(uint64_t) * kDescWords * B);
   L.jflag = take(sizeof(uint32_t) * 2 * static_cast<size_t>(B));
   L.part1 = take(sizeof(Part) * rows * c1);
@@ -202,16 +257,38 @@ struct Params {
   int32_t *out_nacc;
   sv_diag diag;
   Header *hdr;
-  int *row_start;    // [B+1] first flat row of each request
-  float *cs;         // [B] log2(e) / T (0: greedy)
-  uint32_t *k1_cnt;  // [B] row-statistics chunks completed
-  uint32_t *k2_cnt;  // [B] residual chunks completed
+  int tables_global;  // kernel 0 wrote row_start and cs (else each CTA builds them)
+  int *row_start;    // [B+1] first flat row of each request (kernel 0)
+  float *cs;         // [B] log2(e) / T, 0 for greedy (kernel 0)
+  uint32_t *k1_cnt;  // [2][B] row-statistics chunks completed, per counter set
+  uint32_t *k2_cnt;  // [2][B] residual chunks completed, per counter set
   uint64_t *desc;    // [B][kDescWords] rows to re-sample, in reservation (merge) order
-  uint32_t *jflag;   // [2B] kJobWait / kJobDue / kJobNone per job
+  uint32_t *jflag;   // [2B] tagged kJobDue / kJobNone per job
   Part *part1;
   float2 *csum;      // [slot][C2] residual and p sums per chunk
   float2 *ssum;      // [slot][nseg] residual and p sums per 1024-element segment
 };
+
+// Warp-wide: clear counter set s (counters, per-request arrival counts and
+// the set's error word) for a batch of B requests.
+__device__ __forceinline__ void clear_set(const Params &p, int s, int lane) {
+  uint32_t *c = reinterpret_cast<uint32_t *>(&p.hdr->set[s]);
+  for (int i = lane; i < static_cast<int>(sizeof(Counters) / 4); i += 32) c[i] = 0u;
+  uint32_t *k1 = p.k1_cnt + static_cast<size_t>(s) * p.B;
+  uint32_t *k2 = p.k2_cnt + static_cast<size_t>(s) * p.B;
+  for (int i = lane; i < p.B; i += 32) {
+    k1[i] = 0u;
+    k2[i] = 0u;
+  }
+  if (lane == 0) p.hdr->err[s] = 0u;
+}
+
+// Warp-wide: clear every job flag and descriptor word, so that no leftover
+// value of a fresh or foreign workspace can carry a current tag.
+__device__ __forceinline__ void clear_tags(const Params &p, int lane) {
+  for (int i = lane; i < 2 * p.B; i += 32) p.jflag[i] = 0u;
+  for (size_t i = lane; i < static_cast<size_t>(p.B) * kDescWords; i += 32) p.desc[i] = 0ull;
+}
 
 // Input checks shared by the kernels.
 __device__ __forceinline__ bool valid_uniform(float u) { return u >= 0.f && u < 1.f; }

@@ -243,9 +243,10 @@ __device__ __forceinline__ int cdf_block8(int n, const float (&w)[8], float targ
 // elements.  Longer rows walk chunk sums, segment sums, then elements.
 // Warp-wide: slot sl's descriptor, read (and waited for) by lane 0 and handed
 // to every lane; false if the wait gave up.
-__device__ __forceinline__ bool desc_read_warp(const Params &p, int sl, int lane, Desc &d) {
+__device__ __forceinline__ bool desc_read_warp(const Params &p, const Ctl &c, int sl, int lane,
+                                               Desc &d) {
   bool ok = true;
-  if (lane == 0) ok = desc_read(p.desc + static_cast<size_t>(sl) * kDescWords, d, &p.hdr->err);
+  if (lane == 0) ok = desc_read(p.desc + static_cast<size_t>(sl) * kDescWords, d, c.tag, c.err);
   if (!__shfl_sync(kFull, ok ? 1 : 0, 0)) return false;
   uint32_t *f = reinterpret_cast<uint32_t *>(&d);
 #pragma unroll
@@ -256,7 +257,7 @@ __device__ __forceinline__ bool desc_read_warp(const Params &p, int sl, int lane
 // The search of slot sl.  The segment sums depend on the slot alone, so
 // their loads go out before the descriptor is read: both round trips overlap.
 template <typename T, bool kVec>
-__device__ __noinline__ void search_request(const Params &p, int sl, int lane) {
+__device__ __noinline__ void search_request(const Params &p, const Ctl ctl, int sl, int lane) {
   const float2 *cs2 = p.csum + static_cast<size_t>(sl) * p.C2;
   const float2 *ss2 = p.ssum + static_cast<size_t>(sl) * p.nseg;
   const int nsr = (p.V + kSeg - 1) / kSeg;  // segments of the row
@@ -270,7 +271,7 @@ __device__ __noinline__ void search_request(const Params &p, int sl, int lane) {
       wr[j] = v.x;
       wp[j] = v.y;
     }
-    if (!desc_read_warp(p, sl, lane, d)) return;
+    if (!desc_read_warp(p, ctl, sl, lane, d)) return;
     float lr = 0.f, lp = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -294,7 +295,7 @@ __device__ __noinline__ void search_request(const Params &p, int sl, int lane) {
     return;
   }
 
-  if (!desc_read_warp(p, sl, lane, d)) return;
+  if (!desc_read_warp(p, ctl, sl, lane, d)) return;
   // Totals of the residual and of p, in the same scan order the walk uses.
   float tr = 0.f, tp = 0.f;
   float2 v0 = make_float2(0.f, 0.f), v1 = v0;

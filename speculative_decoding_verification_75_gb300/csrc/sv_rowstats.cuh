@@ -200,9 +200,36 @@ __device__ __forceinline__ ChunkStat combine_halves(ChunkStat a, ChunkStat b, fl
 // Counts a finished merge (after its reservation and flags); the last one
 // raises all_merged, after which b_reserved is final for whoever acquires
 // the flag.
-__device__ __forceinline__ void count_merged(const Params &p) {
-  if (atomic_add_acq_rel(&p.hdr->n_merged, 1u) + 1u == ld_cg(&p.hdr->n_valid))
-    st_release(&p.hdr->all_merged, 1u);
+__device__ __forceinline__ void count_merged(const Params &p, const Ctl &c) {
+  if (atomic_add_acq_rel(&c.ctr->n_merged, 1u) + 1u == static_cast<uint32_t>(p.B))
+    st_release(&c.ctr->all_merged, 1u);
+}
+
+// Outputs of a request whose draft length is invalid (it has no rows): -1
+// tokens and num_accepted, NaN / flag 2 diagnostics; counted as finished.
+__device__ void fill_bad_request(const Params &p, const Ctl &c, int b) {
+  const int R = p.gmax + 1;
+  const float qnan = __int_as_float(0x7fc00000);
+  for (int i = 0; i < R; ++i) p.out_tokens[static_cast<size_t>(b) * R + i] = -1;
+  p.out_nacc[b] = -1;
+  const sv_diag &d = p.diag;
+  for (int i = 0; i < p.gmax; ++i) {
+    const size_t pi = static_cast<size_t>(b) * p.gmax + i;
+    if (d.p_tok) d.p_tok[pi] = qnan;
+    if (d.q_tok) d.q_tok[pi] = qnan;
+    if (d.accept_prob) d.accept_prob[pi] = qnan;
+    if (d.flags) d.flags[pi] = 2;
+  }
+  for (int i = 0; i < R; ++i) {
+    const size_t ri = static_cast<size_t>(b) * R + i;
+    if (d.row_max) d.row_max[ri] = qnan;
+    if (d.row_sum) d.row_sum[ri] = qnan;
+    if (d.row_argmax) d.row_argmax[ri] = -1;
+  }
+  if (d.resid_mass) d.resid_mass[b] = qnan;
+  atomicOr(c.err, SV_BAD_DRAFT_LEN);
+  if (d.accept_hist) atomicAdd(d.accept_hist + p.gmax + 1, 1);
+  count_merged(p, c);
 }
 
 constexpr int kMergeBatch = 16;
@@ -213,7 +240,8 @@ constexpr int kMergeBatch = 16;
 // draft ids and uniforms, the first kMergeBatch chunk statistics of each
 // row), then the two gathers that need the draft id (l_x and q(x)).
 template <typename T>
-__device__ __noinline__ void merge_request(const Params &p, int b, int nr, float cs, int lane) {
+__device__ __noinline__ void merge_request(const Params &p, const Ctl c, int b, int nr, float cs,
+                                          int lane) {
   const int g = nr - 1;
   const int R = p.gmax + 1;
   const bool greedy = (cs == 0.f);
@@ -224,7 +252,7 @@ __device__ __noinline__ void merge_request(const Params &p, int b, int nr, float
   // A sampled request reserves its descriptor slot first, so the round trip
   // overlaps the loads below; a slot left unused is flagged kReadySkip.
   uint32_t pos = 0;
-  if (!greedy && lane == 0) pos = atomicAdd(&p.hdr->b_reserved, 1u);
+  if (!greedy && lane == 0) pos = atomicAdd(&c.ctr->b_reserved, 1u);
   // Request-level inputs (the tutorial page, §5.2, takes valid inputs for
   // granted; invalid ones mark only this request).
   const float t = __ldg(p.temp + b);
@@ -384,13 +412,13 @@ __device__ __noinline__ void merge_request(const Params &p, int b, int nr, float
     }
     if (lane == 0) {
       p.out_nacc[b] = -1;
-      atomicOr(&p.hdr->err, bad);
+      atomicOr(c.err, bad);
       if (!greedy) {  // the reserved slot holds nothing: no residual, no search
-        p.jflag[p.B + pos] = kJobNone;
-        desc_publish(p.desc + static_cast<size_t>(pos) * kDescWords, Desc{}, kReadySkip);
+        p.jflag[p.B + pos] = c.tag | kJobNone;
+        desc_publish(p.desc + static_cast<size_t>(pos) * kDescWords, Desc{}, c.tag | kReadySkip);
       }
       if (dg.accept_hist) atomicAdd(dg.accept_hist + p.gmax + 1, 1);
-      count_merged(p);
+      count_merged(p, c);
     }
     return;
   }
@@ -413,7 +441,7 @@ __device__ __noinline__ void merge_request(const Params &p, int b, int nr, float
     d.inv_s = 1.f / sk;
     d.cs = cs;
     d.u = us;
-    desc_publish(p.desc + static_cast<size_t>(pos) * kDescWords, d, kReadySample);
+    desc_publish(p.desc + static_cast<size_t>(pos) * kDescWords, d, c.tag | kReadySample);
   }
   for (int i = lane; i < R; i += 32) {
     int tk = -1;
@@ -424,7 +452,7 @@ __device__ __noinline__ void merge_request(const Params &p, int b, int nr, float
   if (lane == 0) {
     p.out_nacc[b] = k;
     if (dg.accept_hist) atomicAdd(dg.accept_hist + k, 1);
-    count_merged(p);
+    count_merged(p, c);
   }
 }
 

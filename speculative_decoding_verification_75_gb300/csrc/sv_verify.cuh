@@ -85,6 +85,15 @@ constexpr int kWarpProducer = 0, kWarpClaimer = 1, kWarpConsumer0 = 2;
 constexpr int kWarpCounter = kWarpConsumer0 + 2 * kPairs, kWarpJob = kWarpCounter + 1;
 constexpr int kThreads = 32 * (kWarpJob + 1);
 constexpr int kSmemReq = 2048;  // requests whose row offsets and scales sit in shared memory
+constexpr int kTableWarps = kWarpJob + 1 - kWarpConsumer0;  // warps that build them
+constexpr int kTableThreads = 32 * kTableWarps;
+constexpr int kScanPer = (kSmemReq + kTableThreads - 1) / kTableThreads;
+constexpr uint32_t kRoles = 2 + 2 * kPairs + 2;  // producer, claimer, consumers, counter, job
+
+// Named barrier 1 over the table-building warps.
+__device__ __forceinline__ void table_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kTableThreads) : "memory");
+}
 constexpr int kRunRing = 32;
 static_assert(kStages % kPairs == 0, "each consumer pair owns whole stages");
 static_assert(kRunRing > kStages + 1, "every open run fits (each holds an unobserved item)");
@@ -95,8 +104,9 @@ struct Item {
   int ne;     // elements in the chunk
   int has_q;  // residual item reads a q chunk
   int slot;   // row statistics: padded row index; residual: descriptor slot
-  float cs;   // row statistics: log2(e) / T (0: greedy)
-  int pad[2];
+  float cs;   // row statistics with tables in global memory: log2(e) / T (0: greedy)
+  int b;      // row statistics: request
+  int pad;
   Desc d;     // residual item: the row and its statistics
 };
 
@@ -143,11 +153,18 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
   __shared__ uint64_t xbar_s[kStages];  // ... and the barrier that hands it over
   __shared__ int row_start_s[kSmemReq + 1];
   __shared__ float cs_s[kSmemReq];
+  __shared__ int wsum_s[kTableWarps];
+  __shared__ Ctl ctl_s;            // the call's counter set, once the header is checked
+  __shared__ uint64_t ctl_bar_s;   // completes when ctl_s is written
+  __shared__ uint64_t tab_bar_s;   // completes when the shared tables are built
+  __shared__ uint32_t err_s;       // this CTA's SV_FAULT_* bits (flushed when it leaves)
+  __shared__ uint32_t left_s;      // roles of this CTA that have finished
   auto *svcq = &svcq_s;
   auto *clq = &clq_s;
   Item *info = reinterpret_cast<Item *>(smem + kStages * kStageBytes);
   uint64_t *bars = reinterpret_cast<uint64_t *>(info + kStages);
   const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kStages);
+  const uint32_t ctl_bar = smem_addr(&ctl_bar_s), tab_bar = smem_addr(&tab_bar_s);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int R = p.gmax + 1;
   constexpr int kRowChunk = Tiling<T>::kRowChunk;
@@ -159,41 +176,164 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
       mbar_init(empty0 + 8 * s, 2);  // both warps of the owning pair
     }
     for (int s = 0; s < kStages; ++s) mbar_init(smem_addr(&xbar_s[s]), 1);
+    mbar_init(ctl_bar, 1);
+    mbar_init(tab_bar, 1);
     svc_init(svcq);
     svc_init(clq);
+    err_s = 0u;
+    left_s = 0u;
     fence_mbar_init();
   }
-  pdl_wait();  // kernel 0's row offsets, scales and reset counters
-  // The next step's kernel 0 may become resident beside this CTA; it waits
-  // for this grid's completion before it touches the workspace.
-  pdl_launch_dependents();
-  // The claimer's first row claim needs neither the staged tables nor the
-  // barrier: its round trips overlap them.
-  uint32_t n_row_items = 0, rb = 1, a_first = 0;
-  if (warp == kWarpClaimer && lane == 0) {
-    n_row_items = ld_cg(&p.hdr->n_rows) * static_cast<uint32_t>(p.C1);
-    rb = min(static_cast<uint32_t>(kRowBlock), max(1u, n_row_items / (2u * gridDim.x)));
-    a_first = atomicAdd(&p.hdr->a_next, rb);
-  }
-  const bool smem_req = p.B <= kSmemReq;
-  if (smem_req) {
-    for (int i = threadIdx.x; i <= p.B; i += kThreads) row_start_s[i] = ld_cg(p.row_start + i);
-    for (int i = threadIdx.x; i < p.B; i += kThreads) cs_s[i] = ld_cg(p.cs + i);
-  }
   __syncthreads();
+  pdl_wait();  // the inputs, and the workspace as the previous call left it
+  // The next call's grid may become resident as CTAs of this one leave; it
+  // waits for this grid's completion before it reads anything.
+  pdl_launch_dependents();
 
+  uint32_t *err = &err_s;
+  const bool uniform = p.lens == nullptr;       // every request has gmax + 1 rows
+  const bool smem_req = p.tables_global == 0;  // per-CTA tables in shared memory
   const T *logits = static_cast<const T *>(p.logits);
-  uint32_t *err = &p.hdr->err;
-  auto row_start = [&](int b) { return smem_req ? row_start_s[b] : ld_cg(p.row_start + b); };
+  auto row_start = [&](int b) {
+    return uniform ? b * R : (smem_req ? row_start_s[b] : ld_cg(p.row_start + b));
+  };
   auto scale = [&](int b) { return smem_req ? cs_s[b] : ld_cg(p.cs + b); };
-  auto search_slot = [&](int sl) { search_request<T, kTMA>(p, sl, lane); };
+  auto wait_ctl = [&]() -> Ctl {  // the call's counter set (ctr null: the wait gave up)
+    Ctl c{};
+    if (mbar_wait(ctl_bar, 0u, err)) c = ctl_s;
+    return c;
+  };
+  // Each role's lane 0 calls this once when the role is done.  The CTA's
+  // last role hands its wait faults to the call's error word and counts the
+  // CTA out; the grid's last CTA advances the epoch for the next call.  A
+  // fault also withdraws both certificates, so the next call re-clears.
+  auto leave = [&]() {
+    if (atomicAdd(&left_s, 1u) != kRoles - 1) return;
+    const Ctl c = wait_ctl();
+    const uint32_t f = atomicOr(&err_s, 0u);
+    if (c.ctr && f) atomicOr(c.err, f);
+    if (f || !c.ok) {
+      st_relaxed64(&p.hdr->ready[0], 0ull);
+      st_relaxed64(&p.hdr->ready[1], 0ull);
+    }
+    if (c.ctr && atomicAdd(&c.ctr->exited, 1u) == gridDim.x - 1)
+      st_relaxed(&p.hdr->epoch, c.epoch + 1u);
+  };
+
+  if (warp >= kWarpConsumer0) {
+    // ----------------------------------------------- per-CTA tables ----
+    // Softmax scales (and, for ragged drafts, first rows) of every request,
+    // built by the ten warps that do not stream; the producer and claimer
+    // start the first block meanwhile.
+    const int tt = threadIdx.x - 32 * kWarpConsumer0, tw = warp - kWarpConsumer0;
+    uint64_t hdr0 = 0, rdy0 = 0, rdy1 = 0;
+    if (warp == kWarpJob && lane == 0) {  // the header, in flight during the tables
+      hdr0 = ld_relaxed64(reinterpret_cast<const uint64_t *>(&p.hdr->epoch));
+      rdy0 = ld_relaxed64(&p.hdr->ready[0]);
+      rdy1 = ld_relaxed64(&p.hdr->ready[1]);
+    }
+    if (smem_req) {
+      for (int b = tt; b < p.B; b += kTableThreads) {
+        const float t = __ldg(p.temp + b);
+        cs_s[b] = (t > 0.f) ? kLog2e / t : 0.f;
+      }
+      if (!uniform) {  // exclusive scan of the row counts
+        int v[kScanPer], sum = 0;
+#pragma unroll
+        for (int j = 0; j < kScanPer; ++j) {
+          const int b = tt * kScanPer + j;
+          v[j] = b < p.B ? request_rows(p, b) : 0;
+          sum += v[j];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(kFull, incl, o);
+          if (lane >= o) incl += n;
+        }
+        if (lane == 31) wsum_s[tw] = incl;
+        table_sync();
+        int run = incl - sum;
+        for (int w = 0; w < tw; ++w) run += wsum_s[w];
+#pragma unroll
+        for (int j = 0; j < kScanPer; ++j) {
+          const int b = tt * kScanPer + j;
+          if (b < p.B) row_start_s[b] = run;
+          run += v[j];
+        }
+        if (tt == kTableThreads - 1) row_start_s[p.B] = run;
+      }
+    }
+    table_sync();
+    if (tt == 0) mbar_arrive(tab_bar);
+
+    if (warp == kWarpJob) {
+      // ------------------------------------------ the call's counters ----
+      // Set e & 1 serves the call with epoch e once its certificate says
+      // so; otherwise CTA 0 clears it (and every tag) while the others wait.
+      // CTA 0 then clears the other set for the next call.
+      uint32_t e = static_cast<uint32_t>(__shfl_sync(kFull, static_cast<uint32_t>(hdr0), 0));
+      const uint64_t r0 = __shfl_sync(kFull, rdy0, 0), r1 = __shfl_sync(kFull, rdy1, 0);
+      const int s = static_cast<int>(e & 1u);
+      const uint64_t key = certificate(p.B, p.gmax, p.V, e);
+      bool ok = true;
+      if ((s ? r1 : r0) != key) {
+        if (blockIdx.x == 0) {
+          clear_set(p, s, lane);
+          clear_tags(p, lane);
+          __syncwarp();
+          if (lane == 0) {
+            __threadfence();
+            st_release64(&p.hdr->ready[s], key);
+          }
+        } else if (lane == 0) {
+          const uint64_t t0 = global_timer_ns();
+          while (ld_acquire64(&p.hdr->ready[s]) != key) {
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+              atomicOr(err, SV_FAULT_TIMEOUT);
+              ok = false;
+              break;
+            }
+            __nanosleep(128);
+          }
+        }
+        ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+      }
+      if (blockIdx.x == 0) {
+        clear_set(p, s ^ 1, lane);
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          st_release64(&p.hdr->ready[s ^ 1], certificate(p.B, p.gmax, p.V, e + 1u));
+        }
+      }
+      if (lane == 0) {
+        Ctl c;
+        c.ctr = &p.hdr->set[s];
+        c.k1 = p.k1_cnt + static_cast<size_t>(s) * p.B;
+        c.k2 = p.k2_cnt + static_cast<size_t>(s) * p.B;
+        c.err = &p.hdr->err[s];
+        c.tag = epoch_tag(e);
+        c.epoch = e;
+        c.ok = ok ? 1u : 0u;  // 0: the set never became clear; nothing may use it
+        ctl_s = c;
+        mbar_arrive(ctl_bar);  // release: ctl_s
+      }
+      __syncwarp();
+    }
+  }
+
+  auto search_slot = [&](const Ctl &c, int sl) { search_request<T, kTMA>(p, c, sl, lane); };
 
   if (warp == kWarpCounter) {
     // --------------------------------------------------- counter warp ----
     // Takes entry k and whatever entries after it are already queued (lane j
     // holds entry k + j), adds all their runs to the global counters at once
-    // and marks the job of every run that completed a request as due.
-    for (uint32_t k = 0;;) {
+    // and marks the job of every run that completed a request as due.  The
+    // completing add also clears the counter (nobody adds to it again in
+    // this call), leaving the set as the call after next expects it.
+    const Ctl c = wait_ctl();
+    for (uint32_t k = 0; c.ok;) {
       if (!mbar_wait_warp(smem_addr(&svcq->full[k % kSvcSlots]), (k / kSvcSlots) & 1u, err))
         break;
       const uint32_t kj = k + lane;
@@ -208,19 +348,20 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
       k += nb;
       bool last = false;
       if (e.kind >= 0) {
-        uint32_t *cnt = e.kind == 0 ? p.k1_cnt + e.id : p.k2_cnt + e.id;
+        uint32_t *cnt = e.kind == 0 ? c.k1 + e.id : c.k2 + e.id;
         const uint32_t total = e.kind == 0 ? static_cast<uint32_t>(e.nr * p.C1)
                                            : static_cast<uint32_t>(p.C2);
         // Release: the run's results (observed by the producer); acquire:
         // every earlier run's, when this one completes the count.
         last = atomic_add_acq_rel(cnt, static_cast<uint32_t>(e.count)) + e.count == total;
+        if (last) st_relaxed(cnt, 0u);
       }
       // Job due: the merge of request id, or the search of slot id; the
       // release carries every run's results to the job warp that sees it.
       if (last) {
         uint32_t *flag = p.jflag + (e.kind == 0 ? 0 : p.B) + e.id;
-        if (kLocal) st_relaxed(flag, kJobNone);
-        else st_release(flag, kJobDue);
+        if (kLocal) st_relaxed(flag, c.tag | kJobNone);
+        else st_release(flag, c.tag | kJobDue);
       }
       if constexpr (kLocal) {  // run the completed jobs here, one after another
         for (unsigned lm = __ballot_sync(kFull, last); lm; lm &= lm - 1) {
@@ -228,14 +369,16 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
           const int kind = __shfl_sync(kFull, e.kind, src), id = __shfl_sync(kFull, e.id, src);
           __syncwarp();  // lane src's acquire orders every lane's reads
           if (kind == 0) {
-            merge_request<T>(p, id, row_start(id + 1) - row_start(id), scale(id), lane);
+            merge_request<T>(p, c, id, row_start(id + 1) - row_start(id), scale(id), lane);
           } else {
-            search_slot(id);
+            search_slot(c, id);
           }
         }
       }
       if (__any_sync(kFull, e.kind == -1)) break;
     }
+    __syncwarp();
+    if (lane == 0) leave();
     return;
   }
 
@@ -245,24 +388,27 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
     // searches slot s.  A ticket waits until its job is due or will never
     // be (a request without rows, a slot left unused, or -- once every
     // request is merged -- a slot never reserved).
+    const Ctl c = wait_ctl();
     const uint32_t njobs = 2u * static_cast<uint32_t>(p.B);
-    for (;;) {
-      int state = 0;  // 1 due, 2 none (next ticket), 3 no more jobs or timeout
+    const uint32_t due = c.tag | kJobDue, none = c.tag | kJobNone;
+    for (; c.ok;) {
+      int state = 0;  // 1 due, 2 none (next ticket), 3 no more jobs or timeout, 4 no rows
       uint32_t h = 0;
       if (lane == 0) {
-        h = atomicAdd(&p.hdr->jq_head, 1u);
+        h = atomicAdd(&c.ctr->jq_head, 1u);
         if (h >= njobs) state = 3;
+        else if (h < static_cast<uint32_t>(p.B) && row_start(h + 1) == row_start(h)) state = 4;
         const uint64_t t0 = global_timer_ns();
         // Acquire polls of the flag (no separate fence once it is seen).
         while (state == 0) {
           const uint32_t f = ld_acquire(p.jflag + h);  // pairs with the counter's release
-          if (f == kJobDue) {
+          if (f == due) {
             state = 1;
-          } else if (f == kJobNone) {
+          } else if (f == none) {
             state = 2;
-          } else if (h >= static_cast<uint32_t>(p.B) && ld_relaxed(&p.hdr->all_merged) != 0u) {
+          } else if (h >= static_cast<uint32_t>(p.B) && ld_relaxed(&c.ctr->all_merged) != 0u) {
             fence_acq_rel();  // b_reserved is final now
-            if (h - p.B >= ld_relaxed(&p.hdr->b_reserved)) state = 3;
+            if (h - p.B >= ld_relaxed(&c.ctr->b_reserved)) state = 3;
           } else if (global_timer_ns() - t0 > kWaitLimitNs) {
             atomicOr(err, SV_FAULT_TIMEOUT);
             state = 3;
@@ -270,19 +416,22 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
             __nanosleep(kPollNs);
           }
         }
+        if (state == 4) fill_bad_request(p, c, static_cast<int>(h));
       }
       __syncwarp();  // lane 0's acquire of the flag orders every lane's reads
       state = __shfl_sync(kFull, state, 0);
       if (state == 3) break;
-      if (state == 2) continue;
+      if (state != 1) continue;
       const int id = static_cast<int>(__shfl_sync(kFull, h, 0));
       if (id < p.B) {
         const int rows = row_start(id + 1) - row_start(id);
-        merge_request<T>(p, id, rows, scale(id), lane);
+        merge_request<T>(p, c, id, rows, scale(id), lane);
       } else {
-        search_slot(id - p.B);
+        search_slot(c, id - p.B);
       }
     }
+    __syncwarp();
+    if (lane == 0) leave();
     return;
   }
 
@@ -299,16 +448,33 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
     // row is claimed, every request merged and every ticket resolved.  A
     // ticket past the last reserved slot, once every request is merged, ends
     // the stream.  Row blocks are claimed one ahead, so the claim's round
-    // trip overlaps the queueing of the block before.
-    const uint32_t C2 = static_cast<uint32_t>(p.C2);
-    // Claim sizes (rb: set above): up to kRowBlock / kResBlock items, fewer
-    // when the batch is small, so that its items spread over the grid.
-    const uint32_t spread = 2u * gridDim.x;
-    const uint32_t rt = min(static_cast<uint32_t>(kResBlock),
-                            max(1u, ld_cg(&p.hdr->n_valid) * C2 / spread));
-    uint32_t k = 0;
+    // trip overlaps the queueing of the block before.  The first block is
+    // static (block i of CTA i): it needs no counter, so it goes out before
+    // the workspace header is even read.
     bool ok = true;
-    auto push = [&](const Claim &c) { ok = ok && svc_push(clq, k++, c, err); };
+    if (!uniform && smem_req) ok = mbar_wait(tab_bar, 0u, err);  // ragged: the row table
+    const uint32_t n_rows = uniform ? static_cast<uint32_t>(p.B) * R
+                                    : static_cast<uint32_t>(row_start(p.B));
+    const uint32_t n_row_items = n_rows * static_cast<uint32_t>(p.C1);
+    const uint32_t rb =
+        min(static_cast<uint32_t>(kRowBlock), max(1u, n_row_items / (2u * gridDim.x)));
+    const uint32_t a_dyn = rb * gridDim.x;  // first item handed out by the counter
+    const uint32_t C2 = static_cast<uint32_t>(p.C2);
+    // Claim sizes: up to kRowBlock / kResBlock items, fewer when the batch
+    // is small, so that its items spread over the grid.
+    const uint32_t spread = 2u * gridDim.x;
+    const uint32_t rt =
+        min(static_cast<uint32_t>(kResBlock), max(1u, static_cast<uint32_t>(p.B) * C2 / spread));
+    uint32_t k = 0;
+    auto push = [&](const Claim &cl) { ok = ok && svc_push(clq, k++, cl, err); };
+    uint32_t a_cur = rb * blockIdx.x;
+    if (ok && a_cur < n_row_items) {
+      push(Claim{0, a_cur, min(a_cur + rb, n_row_items), 0, 0, 0, {0, 0}, Desc{}});
+      a_cur = n_row_items;  // the next row block comes from the counter
+    }
+    const Ctl c = wait_ctl();
+    ok = ok && c.ok;
+    if (ok) a_cur = a_dyn + atomicAdd(&c.ctr->a_next, rb);
     // Slot s: kReadySample (d holds its descriptor) or kReadySkip once
     // written; 0 when it will never be (every request merged, fewer slots
     // reserved) or on a timeout.
@@ -316,12 +482,12 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
       if (sl >= static_cast<uint32_t>(p.B)) return 0u;  // at most one slot per request
       const uint64_t t0 = global_timer_ns();
       for (;;) {  // relaxed polls of the slot's eight words
-        const uint32_t f = desc_poll(p.desc + static_cast<size_t>(sl) * kDescWords, d);
+        const uint32_t f = desc_poll(p.desc + static_cast<size_t>(sl) * kDescWords, d, c.tag);
         if (f != kPending) return f;
         // All merged: every reservation is visible, b_reserved is final.
-        if (ld_relaxed(&p.hdr->all_merged) != 0u) {
+        if (ld_relaxed(&c.ctr->all_merged) != 0u) {
           fence_acq_rel();
-          if (sl >= ld_relaxed(&p.hdr->b_reserved)) return 0u;
+          if (sl >= ld_relaxed(&c.ctr->b_reserved)) return 0u;
         }
         if (global_timer_ns() - t0 > kWaitLimitNs) {
           atomicOr(err, SV_FAULT_TIMEOUT);
@@ -331,23 +497,22 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
         if (kPollNs) __nanosleep(kPollNs);
       }
     };
-    uint32_t a_cur = a_first;
     bool rows_left = true, more = true;
     while (ok && more) {
       if (rows_left) {
-        const uint2 bc = ld_relaxed2(&p.hdr->b_next);  // {b_next, b_reserved}
+        const uint2 bc = ld_relaxed2(&c.ctr->b_next);  // {b_next, b_reserved}
         const uint32_t sl = bc.x / C2;
         if (sl < bc.y) {
           Desc d;
-          const uint32_t f = desc_poll(p.desc + static_cast<size_t>(sl) * kDescWords, d);
+          const uint32_t f = desc_poll(p.desc + static_cast<size_t>(sl) * kDescWords, d, c.tag);
           const uint32_t s_end = (sl + 1) * C2;
           if (f == kReadySkip) {
-            atomicMax(&p.hdr->b_next, s_end);
+            atomicMax(&c.ctr->b_next, s_end);
             continue;
           }
           if (f == kReadySample) {
             const uint32_t want = min(bc.x + rt, s_end);
-            if (atomicCAS(&p.hdr->b_next, bc.x, want) == bc.x) {  // d is complete
+            if (atomicCAS(&c.ctr->b_next, bc.x, want) == bc.x) {  // d is complete
               const int c0 = static_cast<int>(bc.x - sl * C2);
               push(Claim{1, 0u, 0u, static_cast<int>(sl), c0, c0 + static_cast<int>(want - bc.x),
                          {0, 0}, d});
@@ -356,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
           }
         }
         if (a_cur < n_row_items) {
-          const uint32_t a_pre = atomicAdd(&p.hdr->a_next, rb);
+          const uint32_t a_pre = a_dyn + atomicAdd(&c.ctr->a_next, rb);
           push(Claim{0, a_cur, min(a_cur + rb, n_row_items), 0,
                      0, 0, {0, 0}, Desc{}});
           a_cur = a_pre;
@@ -365,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
         rows_left = false;
       }
       // A ticket: residual items [r, r + rt), slot by slot.
-      const uint32_t r = atomicAdd(&p.hdr->b_next, rt);
+      const uint32_t r = atomicAdd(&c.ctr->b_next, rt);
       for (uint32_t it = r, r_end = r + rt; ok && it < r_end;) {
         const uint32_t sl = it / C2, s_end = (sl + 1) * C2;
         Desc d;
@@ -380,12 +545,15 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
           push(Claim{1, 0u, 0u, static_cast<int>(sl), c0, c0 + static_cast<int>(seg_end - it),
                      {0, 0}, d});
         } else {
-          atomicMax(&p.hdr->b_next, s_end);  // an unused slot: pass it over
+          atomicMax(&c.ctr->b_next, s_end);  // an unused slot: pass it over
         }
         it = seg_end;
       }
     }
-    if (ok) push(Claim{-1, 0u, 0u, 0, 0, 0, {0, 0}, Desc{}});
+    // The end marker goes out whatever happened: the producer and the
+    // consumers stop on it.
+    svc_push(clq, k, Claim{-1, 0u, 0u, 0, 0, 0, {0, 0}, Desc{}}, err);
+    leave();
     return;
   }
 
@@ -395,6 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
     const uint64_t pol_l = policy_evict_normal(), pol_q = policy_evict_first();
     uint32_t n = 0, m = 0, pushed = 0;  // items issued / observed released; runs handed over
     bool ok = true;
+    if (!uniform && smem_req) ok = mbar_wait(tab_bar, 0u, err);  // ragged: the row table
 
     // Open runs, oldest first (head in registers, the rest in a ring).
     Run head{0, 0, 0, 0, 0u};
@@ -460,7 +629,8 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
         rs = re;
         re = row_start(++b + 1);
       }
-      float cs = scale(b);
+      // Scales from shared tables are read by the consumers themselves.
+      float cs = smem_req ? 0.f : scale(b);
       bool fresh = true;
       for (uint32_t it = a; ok && it < a_end; ++it, ++c) {
         if (c == p.C1) {
@@ -470,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
               rs = re;
               re = row_start(++b + 1);
             } while (fr >= re);
-            cs = scale(b);
+            cs = smem_req ? 0.f : scale(b);
             fresh = true;
           }
         }
@@ -489,6 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
         inf.ne = ne;
         inf.slot = slot;
         inf.cs = cs;
+        inf.b = b;
         if (kTMA) {
           const uint32_t bytes = static_cast<uint32_t>(ne) * sizeof(T);
           mbar_arrive_expect_tx(full0 + 8 * s, bytes);
@@ -566,6 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
       info[s].kind = -1;
       mbar_arrive(full0 + 8 * s);
     }
+    leave();
     return;
   }
 
@@ -587,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
     bool ok = true;
     if (kind == 0) {
       const int c = inf.c, ne = inf.ne, slot = inf.slot;
-      const float cs = inf.cs;
+      const float cs = smem_req ? cs_s[inf.b] : inf.cs;
       const int ne0 = half0_len(ne);
       const int off = h ? ne0 : 0, len = h ? ne - ne0 : ne0;
       ChunkStat st;
@@ -640,6 +812,8 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
     if (lane == 0) mbar_arrive(empty0 + 8 * s);  // release: publishes the item's results
     if (!ok) break;
   }
+  __syncwarp();
+  if (lane == 0) leave();
 }
 
 }  // namespace sv
