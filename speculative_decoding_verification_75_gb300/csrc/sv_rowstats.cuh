@@ -234,6 +234,32 @@ __device__ void fill_bad_request(const Params &p, const Ctl &c, int b) {
 
 constexpr int kMergeBatch = 16;
 
+// The inputs of draft position i of request b that the accept test reads:
+// the drafted token x, its uniform u, the target logit at x and q_i(x)
+// (loaded only where they are used; an out-of-range x reads entry 0 and is
+// flagged by the merge).
+struct DraftIn {
+  int x;
+  float u, lx, q;
+};
+
+template <typename T>
+__device__ __forceinline__ DraftIn load_draft_inputs(const Params &p, int b, int g, bool greedy,
+                                                     int i) {
+  const bool draft = i < g;
+  const size_t pi = static_cast<size_t>(b) * p.gmax + (draft ? i : 0);
+  DraftIn d;
+  d.x = draft ? __ldg(p.ids + pi) : 0;
+  d.u = draft ? __ldg(p.u_acc + pi) : 0.f;
+  const int xc = (d.x >= 0 && d.x < p.V) ? d.x : 0;
+  d.lx = (draft && !greedy)
+             ? Elem<T>::load(static_cast<const T *>(p.logits),
+                             (static_cast<size_t>(b) * (p.gmax + 1) + i) * p.V + xc)
+             : 0.f;
+  d.q = (draft && p.q) ? __ldg(p.q + pi * p.V + xc) : 1.f;
+  return d;
+}
+
 // The merge + accept step of request b (nr rows), run by one warp once every
 // chunk of its rows is reduced: lane i handles row i.  Its global loads come
 // in two waves only: every input that is known up front (request scalars,
@@ -241,11 +267,10 @@ constexpr int kMergeBatch = 16;
 // row), then the two gathers that need the draft id (l_x and q(x)).
 template <typename T>
 __device__ __noinline__ void merge_request(const Params &p, const Ctl c, int b, int nr, float cs,
-                                          int lane) {
+                                          int lane, bool pre, DraftIn pin) {
   const int g = nr - 1;
   const int R = p.gmax + 1;
   const bool greedy = (cs == 0.f);
-  const T *logits = static_cast<const T *>(p.logits);
   const sv_diag &dg = p.diag;
   const float qnan = __int_as_float(0x7fc00000);
 
@@ -270,21 +295,18 @@ __device__ __noinline__ void merge_request(const Params &p, const Ctl c, int b, 
     const int i = i0 + lane;
     const bool row = i < nr, draft = i < g;
     const size_t pi = static_cast<size_t>(b) * p.gmax + (draft ? i : 0);
-    // Wave 1: draft inputs and chunk statistics.
-    const int x = draft ? __ldg(p.ids + pi) : 0;
-    const float u = draft ? __ldg(p.u_acc + pi) : 0.f;
+    // Wave 1: chunk statistics (and the draft inputs, unless the job warp
+    // gathered them while it waited); wave 2: the gathers at the draft id.
     const Part *pp = p.part1 + (static_cast<size_t>(b) * R + (row ? i : 0)) * p.C1;
     Part q[kMergeBatch];
 #pragma unroll
     for (int tj = 0; tj < kMergeBatch; ++tj)
       q[tj] = (row && tj < p.C1) ? ld_cg(pp + tj) : Part{-INFINITY, 0.f};
-    // Wave 2: the gathers at the draft id.
+    const DraftIn in = (pre && i0 == 0) ? pin : load_draft_inputs<T>(p, b, g, greedy, i);
+    const int x = in.x;
+    const float u = in.u, lx = in.lx, qraw = in.q;
     const bool x_ok = x >= 0 && x < p.V;
     const int xc = x_ok ? x : 0;
-    const float lx =
-        (draft && !greedy) ? Elem<T>::load(logits, (static_cast<size_t>(b) * R + i) * p.V + xc)
-                           : 0.f;
-    const float qraw = (draft && p.q) ? __ldg(p.q + pi * p.V + xc) : 1.f;
     if (i0 == 0) x0 = x;
 
     float m = -INFINITY, s = 0.f;

@@ -69,12 +69,24 @@ namespace sv {
 #ifndef SV_POLL_NS
 #define SV_POLL_NS 0
 #endif
+#ifndef SV_PREFETCH_NS
+#define SV_PREFETCH_NS 3000
+#endif
+#ifndef SV_ROWS_FIRST
+#define SV_ROWS_FIRST 0
+#endif
 constexpr int kPairs = SV_PAIRS;             // consumer pairs
 constexpr int kStages = SV_STAGES;
 constexpr int kRowBlock = SV_ROW_BLOCK;      // row-statistics items per claim
 constexpr int kResBlock = SV_RES_BLOCK;      // residual items per claim
 constexpr int kClaimSlots = SV_CLAIM_SLOTS;  // claimed blocks queued ahead
 constexpr unsigned kPollNs = SV_POLL_NS;      // pause between polls of a global flag
+constexpr bool kRowsFirst = SV_ROWS_FIRST != 0;  // residual work only once rows are gone
+// A job warp whose merge is not due this long after it took the ticket
+// gathers the merge's draft inputs (ids, uniforms, l(x), q(x)) while it
+// waits, so the merge itself needs one wave of loads.  Early merges never
+// wait that long; the ones that end the step do.
+constexpr uint64_t kPrefetchNs = SV_PREFETCH_NS;
 // Batches of up to this many requests run each merge and search in the
 // counter warp that completes its input (the kernel's kLocal variant), saving the hand-off to another SM's job
 // warp (~1.5 us each) on a step that is one chain of latencies.  With more
@@ -84,7 +96,10 @@ constexpr int kLocalJobsB = SV_LOCAL_JOBS_B;
 constexpr int kWarpProducer = 0, kWarpClaimer = 1, kWarpConsumer0 = 2;
 constexpr int kWarpCounter = kWarpConsumer0 + 2 * kPairs, kWarpJob = kWarpCounter + 1;
 constexpr int kThreads = 32 * (kWarpJob + 1);
-constexpr int kSmemReq = 2048;  // requests whose row offsets and scales sit in shared memory
+#ifndef SV_SMEM_REQ
+#define SV_SMEM_REQ 2048
+#endif
+constexpr int kSmemReq = SV_SMEM_REQ;  // requests whose row offsets and scales sit in shared memory
 constexpr int kTableWarps = kWarpJob + 1 - kWarpConsumer0;  // warps that build them
 constexpr int kTableThreads = 32 * kTableWarps;
 constexpr int kScanPer = (kSmemReq + kTableThreads - 1) / kTableThreads;
@@ -369,7 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
           const int kind = __shfl_sync(kFull, e.kind, src), id = __shfl_sync(kFull, e.id, src);
           __syncwarp();  // lane src's acquire orders every lane's reads
           if (kind == 0) {
-            merge_request<T>(p, c, id, row_start(id + 1) - row_start(id), scale(id), lane);
+            merge_request<T>(p, c, id, row_start(id + 1) - row_start(id), scale(id), lane, false,
+                             DraftIn{});
           } else {
             search_slot(c, id);
           }
@@ -392,40 +408,62 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
     const uint32_t njobs = 2u * static_cast<uint32_t>(p.B);
     const uint32_t due = c.tag | kJobDue, none = c.tag | kJobNone;
     for (; c.ok;) {
-      int state = 0;  // 1 due, 2 none (next ticket), 3 no more jobs or timeout, 4 no rows
+      // 1 due, 2 none (next ticket), 3 no more jobs or timeout, 4 no rows,
+      // 5 gather the draft inputs now
+      int state = 0;
       uint32_t h = 0;
       if (lane == 0) {
         h = atomicAdd(&c.ctr->jq_head, 1u);
         if (h >= njobs) state = 3;
         else if (h < static_cast<uint32_t>(p.B) && row_start(h + 1) == row_start(h)) state = 4;
-        const uint64_t t0 = global_timer_ns();
-        // Acquire polls of the flag (no separate fence once it is seen).
-        while (state == 0) {
-          const uint32_t f = ld_acquire(p.jflag + h);  // pairs with the counter's release
-          if (f == due) {
-            state = 1;
-          } else if (f == none) {
-            state = 2;
-          } else if (h >= static_cast<uint32_t>(p.B) && ld_relaxed(&c.ctr->all_merged) != 0u) {
-            fence_acq_rel();  // b_reserved is final now
-            if (h - p.B >= ld_relaxed(&c.ctr->b_reserved)) state = 3;
-          } else if (global_timer_ns() - t0 > kWaitLimitNs) {
-            atomicOr(err, SV_FAULT_TIMEOUT);
-            state = 3;
-          } else if (kPollNs) {
-            __nanosleep(kPollNs);
-          }
-        }
         if (state == 4) fill_bad_request(p, c, static_cast<int>(h));
       }
-      __syncwarp();  // lane 0's acquire of the flag orders every lane's reads
+      h = __shfl_sync(kFull, h, 0);
       state = __shfl_sync(kFull, state, 0);
+      const int rows = h < static_cast<uint32_t>(p.B) && state == 0
+                           ? row_start(static_cast<int>(h) + 1) - row_start(static_cast<int>(h))
+                           : 0;
+      bool pre = false, may_pre = rows > 0 && rows <= 32;
+      DraftIn pin{};
+      const uint64_t t0 = global_timer_ns();
+      while (state == 0 || state == 5) {
+        if (state == 5) {  // every lane: its draft position's inputs
+          pin = load_draft_inputs<T>(p, static_cast<int>(h), rows - 1, scale(static_cast<int>(h)) == 0.f,
+                                     lane);
+          pre = true;
+          may_pre = false;
+          state = 0;
+        }
+        if (lane == 0) {
+          // Acquire polls of the flag (no separate fence once it is seen).
+          while (state == 0) {
+            const uint32_t f = ld_acquire(p.jflag + h);  // pairs with the counter's release
+            const uint64_t dt = global_timer_ns() - t0;
+            if (f == due) {
+              state = 1;
+            } else if (f == none) {
+              state = 2;
+            } else if (h >= static_cast<uint32_t>(p.B) && ld_relaxed(&c.ctr->all_merged) != 0u) {
+              fence_acq_rel();  // b_reserved is final now
+              if (h - p.B >= ld_relaxed(&c.ctr->b_reserved)) state = 3;
+            } else if (may_pre && dt > kPrefetchNs) {
+              state = 5;
+            } else if (dt > kWaitLimitNs) {
+              atomicOr(err, SV_FAULT_TIMEOUT);
+              state = 3;
+            } else if (kPollNs) {
+              __nanosleep(kPollNs);
+            }
+          }
+        }
+        __syncwarp();  // lane 0's acquire of the flag orders every lane's reads
+        state = __shfl_sync(kFull, state, 0);
+      }
       if (state == 3) break;
       if (state != 1) continue;
-      const int id = static_cast<int>(__shfl_sync(kFull, h, 0));
+      const int id = static_cast<int>(h);
       if (id < p.B) {
-        const int rows = row_start(id + 1) - row_start(id);
-        merge_request<T>(p, c, id, rows, scale(id), lane);
+        merge_request<T>(p, c, id, rows, scale(id), lane, pre, pin);
       } else {
         search_slot(c, id - p.B);
       }
@@ -500,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
     bool rows_left = true, more = true;
     while (ok && more) {
       if (rows_left) {
-        const uint2 bc = ld_relaxed2(&c.ctr->b_next);  // {b_next, b_reserved}
+        const uint2 bc = kRowsFirst ? make_uint2(0u, 0u) : ld_relaxed2(&c.ctr->b_next);
         const uint32_t sl = bc.x / C2;
         if (sl < bc.y) {
           Desc d;
