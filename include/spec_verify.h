@@ -82,8 +82,9 @@ typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 #define SV_BAD_U_ACCEPT 0x8u     /* an acceptance uniform outside [0, 1)    */
 #define SV_BAD_U_SAMPLE 0x10u    /* the sampling uniform outside [0, 1)     */
 #define SV_BAD_NORMALISER 0x20u  /* non-finite softmax normaliser (T > 0),
-                                    or a row maximum whose value over T, in
-                                    log2 units, is not finite in binary32  */
+                                    or a row maximum m with
+                                    |m * log2(e) / T| >= 2^24 in binary32
+                                    (T too small to form p's exponents)    */
 #define SV_FAULT_TIMEOUT 0x10000u/* a bounded wait inside a kernel gave up  */
 
 /*
@@ -239,6 +240,18 @@ SV_API sv_status sv_kv_rollback(const int32_t *num_accepted, const int32_t *draf
  */
 SV_API sv_status sv_last_error(const void *workspace, sv_stream_t stream,
                         uint32_t *out_word);
+
+/*
+ * Small batches (B <= 32, gamma_max < 16, rows on 16-byte boundaries, a
+ * request's row slices fitting one CTA's shared memory, and every cluster
+ * resident at once) run on the cluster path: one thread-block cluster per
+ * request whose CTAs split the vocabulary and exchange their statistics
+ * through distributed shared memory.  Larger batches run the persistent
+ * kernel.  Both compute the same step; sv_set_small_batch_path(0) sends
+ * every batch to the persistent kernel (process-wide, e.g. to compare the
+ * two), 1 restores the default.  Returns the previous setting.
+ */
+SV_API int sv_set_small_batch_path(int enabled);
 
 /* Static, human-readable name of a status code. */
 SV_API const char *sv_status_string(sv_status status);

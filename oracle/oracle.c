@@ -58,8 +58,15 @@ static const double ORC_Q_FLOOR = 1e-10;
 
 /* log2(e) and the largest finite binary32 value (the range check of the
  * temperature-scaled row maximum). */
-static const double ORC_LOG2E = 1.4426950408889634;
-static const double ORC_FLT_MAX = 3.4028234663852886e38;
+static const float ORC_LOG2E_F = 1.4426950408889634f;
+static const float ORC_EXP_LIMIT = 16777216.0f; /* 2^24 */
+
+/* |fl32(m * fl32(log2(e) / T))| < 2^24, in binary32 arithmetic. */
+static int exponent_range_ok(double m, double T) {
+    volatile float cs = ORC_LOG2E_F / (float)T;
+    volatile float o = (float)m * cs;
+    return fabsf(o) < ORC_EXP_LIMIT;
+}
 
 /* Optional outputs.  Any pointer may be NULL except tokens / num_accepted.
  * Shapes: [B] per request, [B, gmax] per draft position, [B, gmax+1] per row.
@@ -301,11 +308,15 @@ static int verify_range(const void *logits, int is_bf16, const int32_t *draft_id
                 if (T > 0.0 && !(isfinite(row_m[i]) && isfinite(row_s[i])))
                     bad |= ORC_BAD_NORMALISER;
                 /* Reading: the step works on binary32 logits (the pages' fp32
-                 * tensors), so a temperature so small that the row maximum
-                 * over T (in log2 units) leaves the binary32 range is invalid
-                 * data, like a non-finite normaliser. */
-                if (T > 0.0 && isfinite(row_m[i]) &&
-                    !(fabs(row_m[i]) * (ORC_LOG2E / T) < ORC_FLT_MAX))
+                 * tensors) and so in binary32 arithmetic, where p is formed
+                 * from exponents (l - m) * log2(e) / T.  A temperature so
+                 * small that the row maximum in log2 units, m * cs with
+                 * cs = log2(e) / T (both rounded to binary32), reaches 2^24
+                 * in magnitude leaves no binary32 room to form those
+                 * exponents (the rounding error of m * cs alone exceeds 1):
+                 * invalid data, like a non-finite normaliser.  The product is
+                 * taken in binary32, as the step takes it. */
+                if (T > 0.0 && isfinite(row_m[i]) && !exponent_range_ok(row_m[i], T))
                     bad |= ORC_BAD_NORMALISER;
             }
         }

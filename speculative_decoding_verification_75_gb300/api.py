@@ -38,7 +38,7 @@ SV_FAULT_TIMEOUT = 0x10000
 # Every symbol include/spec_verify.h declares.
 EXPORTS = ("sv_workspace_bytes", "spec_verify", "spec_verify_diag",
            "sv_last_error", "sv_status_string", "spec_verify_noalloc", "sv_kv_rollback",
-           "sv_selftest_wait_timeout")
+           "sv_selftest_wait_timeout", "sv_set_small_batch_path")
 
 # Bits of the status word of sv_kv_rollback (include/spec_verify.h).
 SV_KV_FREE_LIST_FULL = 0x1
@@ -93,6 +93,8 @@ def load_library():
     lib.sv_last_error.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint32)]
     lib.sv_status_string.restype = ctypes.c_char_p
     lib.sv_status_string.argtypes = [_I]
+    lib.sv_set_small_batch_path.restype = _I
+    lib.sv_set_small_batch_path.argtypes = [_I]
     lib.sv_selftest_wait_timeout.restype = _I
     lib.sv_selftest_wait_timeout.argtypes = [_P, _P, ctypes.c_uint, _P]
     lib.sv_kv_rollback.restype = _I
@@ -103,6 +105,13 @@ def load_library():
 
 def workspace_bytes(B: int, gamma_max: int, V: int) -> int:
     return int(load_library().sv_workspace_bytes(B, gamma_max, V))
+
+
+def set_small_batch_path(enabled: bool) -> bool:
+    """Route small batches to the cluster kernel (True, the default) or send
+    every batch to the persistent kernel (False), process-wide.  Returns the
+    previous setting."""
+    return bool(load_library().sv_set_small_batch_path(1 if enabled else 0))
 
 
 def status_string(status: int) -> str:

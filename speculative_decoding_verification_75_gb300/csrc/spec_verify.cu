@@ -25,6 +25,7 @@
 #include "sv_device.cuh"
 #include "sv_layout.cuh"
 #include "sv_kv.cuh"
+#include "sv_cluster.cuh"
 #include "sv_prepare.cuh"
 #include "sv_verify.cuh"
 
@@ -56,6 +57,8 @@ __global__ void sv_selftest_wait_kernel(uint32_t *word, const uint32_t *never,
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kClusterMaxB = 32;  // batches up to this size may take the cluster path
+std::atomic<int> g_small_batch_path{1};  // sv_set_small_batch_path
 
 bool sizes_ok(int B, int gmax, int V) {
   if (B < 0 || gmax < 0 || V < 1) return false;
@@ -94,6 +97,86 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
+// ------------------------------------------------ small-batch path ----
+// One cluster of CS CTAs per request (sv_cluster.cuh), when the whole batch
+// fits on the GPU at once: B clusters co-resident, every row slice of a
+// request (plus its q slice) in one CTA's shared memory, gamma_max < 16,
+// rows aligned for TMA.
+constexpr size_t kClusterSmemMax = 220 * 1024;
+constexpr size_t kClusterSmemStep = 8 * 1024;
+constexpr int kClusterSizes[3] = {16, 12, 8};
+
+// Clusters of cs CTAs with smem bytes of dynamic shared memory each that can
+// be resident together, queried once per device, element type, cluster size
+// and 8 KiB class of the footprint (the class's upper end: conservative).
+template <typename T>
+int cluster_capacity(int dev, int cs_index, size_t smem) {
+  constexpr int kClasses = static_cast<int>(kClusterSmemMax / kClusterSmemStep);
+  static std::atomic<int> cache[kMaxDevices][3][kClasses];  // value + 1
+  const int cls = static_cast<int>((smem + kClusterSmemStep - 1) / kClusterSmemStep) - 1;
+  if (cls < 0 || cls >= kClasses) return 0;
+  std::atomic<int> &slot = cache[dev % kMaxDevices][cs_index][cls];
+  int v = slot.load(std::memory_order_acquire);
+  if (v > 0) return v - 1;
+  const int cs = kClusterSizes[cs_index];
+  int n = 0;
+  auto *k = sv_cluster_kernel<T>;
+  bool ok = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kClusterSmemMax)) == cudaSuccess;
+  if (ok && cs > 8)
+    ok = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+  if (ok) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs);
+    cfg.blockDim = dim3(kCThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(cls + 1) * kClusterSmemStep;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();  // a refused size only means: not this path
+  slot.store(n + 1, std::memory_order_release);
+  return n;
+}
+
+// Launches the cluster kernel if the batch qualifies (the largest cluster
+// size whose footprint fits and whose clusters can all be resident); false
+// otherwise.
+template <typename T>
+bool try_cluster(const Params &p, cudaStream_t st, int dev, sv_status *status) {
+  if (p.gmax + 1 > kCMaxRows) return false;
+  for (int ci = 0; ci < 3; ++ci) {
+    const int cs = kClusterSizes[ci];
+    const int W = (p.V + cs - 1) / cs;
+    const int Wr = (W + 7) / 8 * 8;  // 16-byte aligned slices (bf16 and fp32)
+    const size_t smem = cluster_smem_bytes(p.gmax + 1, Wr, sizeof(T));
+    if (smem > kClusterSmemMax || cluster_capacity<T>(dev, ci, smem) < p.B) continue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.B * cs));
+    cfg.blockDim = dim3(kCThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    *status = cudaLaunchKernelEx(&cfg, sv_cluster_kernel<T>, p, Wr) == cudaSuccess ? SV_OK
+                                                                                   : SV_ERR_CUDA;
+    return true;
+  }
+  return false;
+}
+
 template <typename T, bool kTMA>
 sv_status launch_all(Params &p, cudaStream_t st, int dev, int nsm) {
   static std::atomic<uint64_t> smem_done{0}, smem_done_local{0};
@@ -108,9 +191,24 @@ sv_status launch_all(Params &p, cudaStream_t st, int dev, int nsm) {
     return SV_ERR_CUDA;
 
   p.tables_global = p.B > kSmemReq ? 1 : 0;
-  if ((p.tables_global || p.diag.accept_hist) &&
-      launch_pdl(sv_prepare_kernel, dim3(1), dim3(kPrepThreads), 0, st, p) != cudaSuccess)
-    return SV_ERR_CUDA;
+  const bool small = kTMA && p.B <= kClusterMaxB &&
+                     g_small_batch_path.load(std::memory_order_relaxed) != 0;
+  if ((p.tables_global || p.diag.accept_hist) && !small) {
+    if (launch_pdl(sv_prepare_kernel, dim3(1), dim3(kPrepThreads), 0, st, p) != cudaSuccess)
+      return SV_ERR_CUDA;
+  }
+  if (small) {
+    Params pc = p;
+    pc.tables_global = 0;  // the cluster kernel needs no tables
+    if (pc.diag.accept_hist &&
+        launch_pdl(sv_prepare_kernel, dim3(1), dim3(kPrepThreads), 0, st, pc) != cudaSuccess)
+      return SV_ERR_CUDA;
+    sv_status s = SV_OK;
+    if (try_cluster<T>(pc, st, dev, &s)) return s;
+    if (p.tables_global &&
+        launch_pdl(sv_prepare_kernel, dim3(1), dim3(kPrepThreads), 0, st, p) != cudaSuccess)
+      return SV_ERR_CUDA;
+  }
 
   const long long max_items = static_cast<long long>(p.B) * (p.gmax + 1) * p.C1;
   const int grid = static_cast<int>(max_items < nsm ? max_items : nsm);
@@ -255,6 +353,10 @@ sv_status sv_selftest_wait_timeout(uint32_t *word, const uint32_t *never_set,
   sv::sv_selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       word, never_set, static_cast<uint64_t>(limit_us) * 1000u);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+int sv_set_small_batch_path(int enabled) {
+  return sv::g_small_batch_path.exchange(enabled ? 1 : 0);
 }
 
 const char *sv_status_string(sv_status status) {

@@ -181,6 +181,33 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Thread-block clusters: this CTA's rank, the cluster's size, a barrier of
+// every thread of the cluster (release / acquire: shared-memory writes
+// before it are visible to peers after it), and a load from a peer CTA's
+// shared memory (distributed shared memory).
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float2 ld_peer_f2(const void *local, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local)), "r"(rank));
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(ra) : "memory");
+  return v;
+}
+
 // 2^x on the special-function unit (ftz: results below 2^-126 become 0).
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -203,12 +230,18 @@ struct Elem<float> {
   __device__ __forceinline__ static float load(const float *p, size_t i) {
     return __ldg(p + i);
   }
+  // From shared memory (a plain load: the read-only path is global only).
+  __device__ __forceinline__ static float load_shared(const float *p, int i) { return p[i]; }
 };
 
 template <>
 struct Elem<__nv_bfloat16> {
   __device__ __forceinline__ static float load(const __nv_bfloat16 *p, size_t i) {
     const unsigned short h = __ldg(reinterpret_cast<const unsigned short *>(p) + i);
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  }
+  __device__ __forceinline__ static float load_shared(const __nv_bfloat16 *p, int i) {
+    const unsigned short h = reinterpret_cast<const unsigned short *>(p)[i];
     return __uint_as_float(static_cast<uint32_t>(h) << 16);
   }
 };

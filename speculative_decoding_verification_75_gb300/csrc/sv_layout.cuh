@@ -290,6 +290,70 @@ __device__ __forceinline__ void clear_tags(const Params &p, int lane) {
   for (size_t i = lane; i < static_cast<size_t>(p.B) * kDescWords; i += 32) p.desc[i] = 0ull;
 }
 
+// Warp-wide: the call's counter set, from the header words the warp's lane
+// 0 read after the grid dependency wait (epoch and error words, both
+// certificates).  Set e & 1 serves the call with epoch e once its
+// certificate says so; otherwise CTA 0 clears it (and every tag) while the
+// other CTAs wait (bounded: on a timeout ok is 0 and nothing may use the
+// set).  CTA 0 then clears the other set for the next call and certifies
+// it.  Every CTA of the grid must be resident together.
+__device__ __forceinline__ Ctl check_workspace(const Params &p, uint64_t hdr0, uint64_t rdy0,
+                                               uint64_t rdy1, int lane, uint32_t *err) {
+  const uint32_t e = static_cast<uint32_t>(__shfl_sync(kFull, static_cast<uint32_t>(hdr0), 0));
+  const uint64_t r0 = __shfl_sync(kFull, rdy0, 0), r1 = __shfl_sync(kFull, rdy1, 0);
+  const int s = static_cast<int>(e & 1u);
+  const uint64_t key = certificate(p.B, p.gmax, p.V, e);
+  const bool cta0 = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+  bool ok = true;
+  if ((s ? r1 : r0) != key) {
+    if (cta0) {
+      clear_set(p, s, lane);
+      clear_tags(p, lane);
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        st_release64(&p.hdr->ready[s], key);
+      }
+    } else if (lane == 0) {
+      const uint64_t t0 = global_timer_ns();
+      while (ld_acquire64(&p.hdr->ready[s]) != key) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          atomicOr(err, SV_FAULT_TIMEOUT);
+          ok = false;
+          break;
+        }
+        __nanosleep(128);
+      }
+    }
+    ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+  }
+  if (cta0) {
+    clear_set(p, s ^ 1, lane);
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence();
+      st_release64(&p.hdr->ready[s ^ 1], certificate(p.B, p.gmax, p.V, e + 1u));
+    }
+  }
+  Ctl c;
+  c.ctr = &p.hdr->set[s];
+  c.k1 = p.k1_cnt + static_cast<size_t>(s) * p.B;
+  c.k2 = p.k2_cnt + static_cast<size_t>(s) * p.B;
+  c.err = &p.hdr->err[s];
+  c.tag = epoch_tag(e);
+  c.epoch = e;
+  c.ok = ok ? 1u : 0u;
+  return c;
+}
+
+// The header words check_workspace needs (lane 0 of the checking warp).
+__device__ __forceinline__ void read_header(const Params &p, uint64_t &hdr0, uint64_t &rdy0,
+                                            uint64_t &rdy1) {
+  hdr0 = ld_relaxed64(reinterpret_cast<const uint64_t *>(&p.hdr->epoch));
+  rdy0 = ld_relaxed64(&p.hdr->ready[0]);
+  rdy1 = ld_relaxed64(&p.hdr->ready[1]);
+}
+
 // Input checks shared by the kernels.
 __device__ __forceinline__ bool valid_uniform(float u) { return u >= 0.f && u < 1.f; }
 

@@ -242,11 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
     // start the first block meanwhile.
     const int tt = threadIdx.x - 32 * kWarpConsumer0, tw = warp - kWarpConsumer0;
     uint64_t hdr0 = 0, rdy0 = 0, rdy1 = 0;
-    if (warp == kWarpJob && lane == 0) {  // the header, in flight during the tables
-      hdr0 = ld_relaxed64(reinterpret_cast<const uint64_t *>(&p.hdr->epoch));
-      rdy0 = ld_relaxed64(&p.hdr->ready[0]);
-      rdy1 = ld_relaxed64(&p.hdr->ready[1]);
-    }
+    if (warp == kWarpJob && lane == 0)  // the header, in flight during the tables
+      read_header(p, hdr0, rdy0, rdy1);
     if (smem_req) {
       for (int b = tt; b < p.B; b += kTableThreads) {
         const float t = __ldg(p.temp + b);
@@ -284,53 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
 
     if (warp == kWarpJob) {
       // ------------------------------------------ the call's counters ----
-      // Set e & 1 serves the call with epoch e once its certificate says
-      // so; otherwise CTA 0 clears it (and every tag) while the others wait.
-      // CTA 0 then clears the other set for the next call.
-      uint32_t e = static_cast<uint32_t>(__shfl_sync(kFull, static_cast<uint32_t>(hdr0), 0));
-      const uint64_t r0 = __shfl_sync(kFull, rdy0, 0), r1 = __shfl_sync(kFull, rdy1, 0);
-      const int s = static_cast<int>(e & 1u);
-      const uint64_t key = certificate(p.B, p.gmax, p.V, e);
-      bool ok = true;
-      if ((s ? r1 : r0) != key) {
-        if (blockIdx.x == 0) {
-          clear_set(p, s, lane);
-          clear_tags(p, lane);
-          __syncwarp();
-          if (lane == 0) {
-            __threadfence();
-            st_release64(&p.hdr->ready[s], key);
-          }
-        } else if (lane == 0) {
-          const uint64_t t0 = global_timer_ns();
-          while (ld_acquire64(&p.hdr->ready[s]) != key) {
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-              atomicOr(err, SV_FAULT_TIMEOUT);
-              ok = false;
-              break;
-            }
-            __nanosleep(128);
-          }
-        }
-        ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
-      }
-      if (blockIdx.x == 0) {
-        clear_set(p, s ^ 1, lane);
-        __syncwarp();
-        if (lane == 0) {
-          __threadfence();
-          st_release64(&p.hdr->ready[s ^ 1], certificate(p.B, p.gmax, p.V, e + 1u));
-        }
-      }
+      const Ctl c = check_workspace(p, hdr0, rdy0, rdy1, lane, err);
       if (lane == 0) {
-        Ctl c;
-        c.ctr = &p.hdr->set[s];
-        c.k1 = p.k1_cnt + static_cast<size_t>(s) * p.B;
-        c.k2 = p.k2_cnt + static_cast<size_t>(s) * p.B;
-        c.err = &p.hdr->err[s];
-        c.tag = epoch_tag(e);
-        c.epoch = e;
-        c.ok = ok ? 1u : 0u;  // 0: the set never became clear; nothing may use it
         ctl_s = c;
         mbar_arrive(ctl_bar);  // release: ctl_s
       }

@@ -19,7 +19,8 @@ the oracle disagrees with what the speculative-decoding tutorial page
   empty_residual       the reading for sum (p - q)_+ = 0: draw from p
   bad_inputs / ragged / zero_drafts  the documented edge-case contract
   temperature_range    the reading that a temperature so small that the row
-                       maximum over T leaves the binary32 range is invalid
+                       maximum in log2 units, m log2(e) / T, reaches 2^24 in
+                       binary32 is invalid
 
 ``scale`` shrinks the Monte Carlo sizes (the mutation tests use 0.1).
 """
@@ -364,23 +365,30 @@ def pin_zero_drafts(orc, scale=1.0):
 
 
 def pin_temperature_range(orc, scale=1.0):
-    """Reading (the pages' logits are binary32 tensors): a request whose row
-    maximum over T, in log2 units, is not finite in binary32 has invalid
-    data (BAD_NORMALISER = 32), while the same tiny T with a row maximum of
-    0, or a small T that keeps the product finite, is a valid request."""
+    """Reading (the pages' logits are binary32 tensors, so the step runs in
+    binary32): a request whose row maximum in log2 units, m * log2(e) / T,
+    reaches 2^24 in magnitude (product and quotient rounded to binary32) has
+    invalid data (BAD_NORMALISER = 32).  The same tiny T with a row maximum
+    of 0 is a valid, one-hot request; so is a product just below 2^24."""
     V = 4
-    T = np.array([1e-37, 1e-37, 1e-30], np.float32)
-    logits = np.zeros((3, 2, V), np.float32)
-    logits[0] = [[100.0, 1.0, 2.0, 3.0], [100.0, 1.0, 2.0, 3.0]]    # 100 * log2e / 1e-37 >> 3.4e38
-    logits[1] = [[0.0, -1.0, -2.0, -3.0], [0.0, -1.0, -2.0, -3.0]]  # maximum 0: offset 0
-    logits[2] = [[10.0, 1.0, 2.0, 3.0], [10.0, 1.0, 2.0, 3.0]]      # 1.4e31: finite
-    ids = np.zeros((3, 1), np.int32)
-    r = orc.verify(logits, ids, None, np.full((3, 1), 0.5, np.float32),
-                   np.full(3, 0.5, np.float32), T)
-    assert r["bad"].tolist() == [32, 0, 0]
-    assert r["num_accepted"][0] == -1
+    #   m = 100, T = 1e-37: 1.4e39, beyond binary32 altogether
+    #   m = 0,   T = 1e-37: offset 0, every other exponent below -2^24
+    #   m = 10,  T = 1e-30: 1.4e31 >= 2^24
+    #   m = 1,   T = 1e-7:  1.44e7 < 2^24 = 1.68e7
+    #   m = 1,   T = 8e-8:  1.80e7 >= 2^24
+    T = np.array([1e-37, 1e-37, 1e-30, 1e-7, 8e-8], np.float32)
+    top = [100.0, 0.0, 10.0, 1.0, 1.0]
+    logits = np.zeros((5, 2, V), np.float32)
+    for r, m in enumerate(top):
+        logits[r, :, 0] = m
+        logits[r, :, 1:] = m - np.array([1.0, 2.0, 3.0], np.float32)
+    ids = np.zeros((5, 1), np.int32)
+    r = orc.verify(logits, ids, None, np.full((5, 1), 0.5, np.float32),
+                   np.full(5, 0.5, np.float32), T)
+    assert r["bad"].tolist() == [32, 0, 32, 0, 32]
+    assert r["num_accepted"].tolist() == [-1, 1, -1, 1, -1]
     # the valid rows are one-hot at the maximum: draft 0 accepted, bonus 0
-    assert r["tokens"][1].tolist() == [0, 0] and r["tokens"][2].tolist() == [0, 0]
+    assert r["tokens"][1].tolist() == [0, 0] and r["tokens"][3].tolist() == [0, 0]
 
 
 ALL_PINS = [pin_worked_example, pin_lossless, pin_expected_emitted,

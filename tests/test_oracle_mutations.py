@@ -40,7 +40,8 @@ MUTATIONS = {
     "uniform_closed_interval": ("return u >= 0.0 && u < 1.0;", "return u >= 0.0 && u <= 1.0;", 1),
     "no_fallback": ("if (!(S > 0.0)) {", "if (0) {", 1),
     "greedy_ignored": ("if (T == 0.0)\n        return j == argmax ? 1.0 : 0.0;", "", 1),
-    "range_check_dropped": ("!(fabs(row_m[i]) * (ORC_LOG2E / T) < ORC_FLT_MAX)", "0", 1),
+    "range_check_dropped": ("!exponent_range_ok(row_m[i], T)", "0", 1),
+    "range_limit_off": ("return fabsf(o) < ORC_EXP_LIMIT;", "return isfinite(o);", 1),
 }
 
 

@@ -182,23 +182,32 @@ def test_invalid_inputs_are_isolated():
     assert word == 1 | 2 | 4 | 8 | 16 | 32
 
 
-def test_tiny_temperature_is_invalid_data():
-    """A temperature so small that the row maximum over T leaves the binary32
-    range marks the request bad (SV_BAD_NORMALISER), as the oracle does; the
-    same temperature with a row maximum of 0 is a valid (one-hot) request."""
-    B, g, V = 4, 2, 4096
+@pytest.mark.parametrize("V", [4096, 40000])
+@pytest.mark.parametrize("small_path", [True, False], ids=["cluster", "persistent"])
+def test_tiny_temperature_is_invalid_data(V, small_path):
+    """A temperature so small that the row maximum in log2 units reaches 2^24
+    (in binary32) marks the request bad (SV_BAD_NORMALISER), as the oracle
+    does.  The same T with a row maximum of 0 is a valid one-hot request even
+    though the other elements' exponents (and, over several chunks or
+    slices, their own partial sums) leave the binary32 range; a product just
+    below 2^24 is valid too."""
+    B, g = 6, 2
     w = Workload("tinyT", B, g, V, "fp32", 1.0, (0.5, 0.5), (1.0,), seed=17)
     case = make_case(w, device=DEV)
     lg = case["logits"]
     lg[0, :, :] = torch.linspace(-3.0, 100.0, V, device=DEV)   # 100 * log2e / 1e-37 overflows
     lg[1, :, :] = torch.linspace(-3.0, 0.0, V, device=DEV)     # maximum 0: offset 0
-    case["temperature"][0] = 1e-37
-    case["temperature"][1] = 1e-37
-    gpu = run_gpu(case)
+    lg[2, :, :] = torch.linspace(-3.0, 1.0, V, device=DEV)     # 1.44e7 < 2^24
+    lg[3, :, :] = torch.linspace(-3.0, 1.0, V, device=DEV)     # 1.80e7 >= 2^24
+    case["temperature"][0:4] = torch.tensor([1e-37, 1e-37, 1e-7, 8e-8], device=DEV)
+    prev = api.set_small_batch_path(small_path)
+    try:
+        gpu = run_gpu(case)
+    finally:
+        api.set_small_batch_path(prev)
     ora = run_oracle(case)
     compare(case, gpu, ora)
-    assert ora["bad"].tolist()[:2] == [32, 0]
-    assert int(gpu["num_accepted"][0]) == -1 and int(gpu["num_accepted"][1]) >= 0
+    assert ora["bad"].tolist() == [32, 0, 0, 32, 0, 0]
 
 
 def test_no_request_with_rows_ends_cleanly():
