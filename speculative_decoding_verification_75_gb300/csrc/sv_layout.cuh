@@ -100,6 +100,9 @@ __device__ __forceinline__ uint32_t epoch_tag(uint32_t e) { return (e & kEpochMa
 // not (yet) due.  Job b < B merges request b; job B + s searches the
 // residual of descriptor slot s.
 constexpr uint32_t kJobDue = 1u, kJobNone = 2u;
+// An arrival count that marks a descriptor slot whose request turned out
+// invalid (no residual, no search), for job warps that poll the counts.
+constexpr uint32_t kSkipCount = 0xffffffffu;
 
 // State of descriptor slot s (with the call's tag): holds a row to
 // re-sample / holds nothing (its request turned out invalid); any other

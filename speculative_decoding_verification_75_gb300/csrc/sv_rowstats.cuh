@@ -532,6 +532,7 @@ __device__ __noinline__ void merge_request(const Params &p, const Ctl c, int b, 
     if (lane == 0) {
       if (!greedy) {  // the reserved slot holds nothing: no residual, no search
         p.jflag[p.B + pos] = c.tag | kJobNone;
+        c.k2[pos] = kSkipCount;
         desc_publish(p.desc + static_cast<size_t>(pos) * kDescWords, Desc{}, c.tag | kReadySkip);
       }
       count_merged(p, c);

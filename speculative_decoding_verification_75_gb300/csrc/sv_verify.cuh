@@ -29,14 +29,13 @@
 //   consumer pairs  two warps reduce one item together, each half of it
 //                   (chunk statistics or residual sums), and combine;
 //   counter warp    adds completed runs of items to the requests' global
-//                   counters (a batch of runs at once, one per lane) and
-//                   appends a job to the global job queue for each run that
-//                   completed a request;
-//   job warp        takes tickets from the global job queue and runs the
-//                   job it draws: the merge + accept step of a request or
-//                   the inverse-CDF search of its residual.  Jobs go to
-//                   whichever CTA asks next, so they run in parallel across
-//                   the grid whatever CTA completed the requests.
+//                   arrival counters (a batch of runs at once, one per
+//                   lane); a complete count makes a job due;
+//   job warp        takes tickets over the jobs (one merge + accept step
+//                   per request, one inverse-CDF search per drawn row) and
+//                   runs the job it draws once its count is complete.  Jobs
+//                   go to whichever CTA asks next, so they run in parallel
+//                   across the grid whatever CTA completed the requests.
 // Every wait is bounded (about 2 s of %globaltimer); a timeout sets
 // SV_FAULT_TIMEOUT and the CTA leaves in order.
 #pragma once
@@ -296,9 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
     // --------------------------------------------------- counter warp ----
     // Takes entry k and whatever entries after it are already queued (lane j
     // holds entry k + j), adds all their runs to the global counters at once
-    // and marks the job of every run that completed a request as due.  The
-    // completing add also clears the counter (nobody adds to it again in
-    // this call), leaving the set as the call after next expects it.
+    // with one acquire-release add each; the add that completes a count
+    // makes that request's merge (or that slot's search) due.
     const Ctl c = wait_ctl();
     for (uint32_t k = 0; c.ok;) {
       if (!mbar_wait_warp(smem_addr(&svcq->full[k % kSvcSlots]), (k / kSvcSlots) & 1u, err))
@@ -321,16 +319,13 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
         // Release: the run's results (observed by the producer); acquire:
         // every earlier run's, when this one completes the count.
         last = atomic_add_acq_rel(cnt, static_cast<uint32_t>(e.count)) + e.count == total;
-        if (last) st_relaxed(cnt, 0u);
       }
-      // Job due: the merge of request id, or the search of slot id; the
-      // release carries every run's results to the job warp that sees it.
-      if (last) {
-        uint32_t *flag = p.jflag + (e.kind == 0 ? 0 : p.B) + e.id;
-        if (kLocal) st_relaxed(flag, c.tag | kJobNone);
-        else st_release(flag, c.tag | kJobDue);
-      }
-      if constexpr (kLocal) {  // run the completed jobs here, one after another
+      // A job warp sees a completed count itself (its acquire load pairs
+      // with this add); in the kLocal variant this warp runs the job and
+      // flags it taken.  The set's counters are cleared for the call after
+      // next by the next call's CTA 0.
+      if constexpr (kLocal) {  // run the jobs that complete here, one after another
+        if (last) st_relaxed(p.jflag + (e.kind == 0 ? 0 : p.B) + e.id, c.tag | kJobNone);
         for (unsigned lm = __ballot_sync(kFull, last); lm; lm &= lm - 1) {
           const int src = __ffs(lm) - 1;
           const int kind = __shfl_sync(kFull, e.kind, src), id = __shfl_sync(kFull, e.id, src);
@@ -352,11 +347,12 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
 
   if (warp == kWarpJob) {
     // ------------------------------------------------------- job warp ----
-    // Tickets over the 2B job flags: job b < B merges request b, job B + s
-    // searches slot s.  A ticket waits until its job is due or will never
-    // be (a request without rows, a slot left unused, or -- once every
-    // request is merged -- a slot never reserved).
+    // Tickets over 2B jobs: job b < B merges request b, job B + s searches
+    // slot s.  A ticket waits until its job is due -- its arrival count is
+    // complete -- or will never be (a request without rows, a slot left
+    // unused, or -- once every request is merged -- a slot never reserved).
     const Ctl c = wait_ctl();
+    constexpr bool kCounts = !kLocal;  // poll arrival counters (kLocal: flags)
     const uint32_t njobs = 2u * static_cast<uint32_t>(p.B);
     const uint32_t due = c.tag | kJobDue, none = c.tag | kJobNone;
     for (; c.ok;) {
@@ -387,13 +383,24 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
           state = 0;
         }
         if (lane == 0) {
-          // Acquire polls of the flag (no separate fence once it is seen).
+          // Acquire polls of the flag, or of the arrival counter (no separate
+          // fence once the job is seen to be due).
+          const bool merge_job = h < static_cast<uint32_t>(p.B);
+          const uint32_t *poll = !kCounts ? p.jflag + h
+                                 : merge_job ? c.k1 + h
+                                             : c.k2 + (h - p.B);
+          const uint32_t full = !kCounts ? due
+                                : merge_job ? static_cast<uint32_t>(rows * p.C1)
+                                            : static_cast<uint32_t>(p.C2);
+          const uint32_t skip = kCounts ? kSkipCount : none;
           while (state == 0) {
-            const uint32_t f = ld_acquire(p.jflag + h);  // pairs with the counter's release
+            // pairs with the counter warp's release (its flag store, or the
+            // acquire-release add that completed the count)
+            const uint32_t f = ld_acquire(poll);
             const uint64_t dt = global_timer_ns() - t0;
-            if (f == due) {
+            if (f == full) {
               state = 1;
-            } else if (f == none) {
+            } else if (f == skip) {
               state = 2;
             } else if (h >= static_cast<uint32_t>(p.B) && ld_relaxed(&c.ctr->all_merged) != 0u) {
               fence_acq_rel();  // b_reserved is final now
