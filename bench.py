@@ -33,7 +33,7 @@ if str(ROOT) not in sys.path:
 
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
-KERNELS_PER_STEP = 1          # the persistent verification kernel (B <= 2048, no histogram)
+KERNELS_PER_STEP = 1          # one kernel per step (B <= 256 or the cluster path; no histogram)
 METRIC = "verified draft rows/sec"
 UNIT = "rows/s"
 

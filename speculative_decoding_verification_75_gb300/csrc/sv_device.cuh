@@ -113,12 +113,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return pol;
 }
 
-__device__ __forceinline__ uint64_t policy_evict_normal() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
 // 1-D bulk copy global -> shared, completing `bytes` of transaction count on
 // the mbarrier.  src and dst 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void tma_load_1d(uint32_t dst, const void *src,

@@ -19,8 +19,10 @@ namespace sv {
 
 // Every shared-memory stage holds one work item: a row-statistics chunk
 // fills it with logits, a residual chunk with logits plus q (fp32).
+// 27 KiB: eight stages fill the shared memory the tables leave (24 KiB
+// stages measured c3 64.0 vs 63.0 us, c5 114.4 vs 107.8 us).
 #ifndef SV_STAGE_BYTES
-#define SV_STAGE_BYTES 24576
+#define SV_STAGE_BYTES 27648
 #endif
 constexpr int kStageBytes = SV_STAGE_BYTES;
 constexpr int kSeg = 1024;  // elements per residual segment
