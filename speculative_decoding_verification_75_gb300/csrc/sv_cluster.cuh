@@ -46,10 +46,23 @@ __host__ __device__ inline int cluster_warp_range(int ne) {
   return (per + 255) / 256 * 256;
 }
 
-// Dynamic shared memory of the cluster kernel: every row's slice, then the
-// slice of q_k (fp32).
+// Dynamic shared memory of the cluster kernel: one slot of W elements per
+// row.  The slice of q_k (fp32: 4 / esz slots) reuses slots of rows other
+// than k once the row statistics are done; with fewer than 2 * (4 / esz) + 1
+// rows such a run of slots may not exist, and 4 / esz extra slots follow.
+__host__ __device__ inline int cluster_q_slots(int esz) { return 4 / esz; }
+__host__ __device__ inline int cluster_slots(int rows, int esz) {
+  const int ns = cluster_q_slots(esz);
+  return rows >= 2 * ns + 1 ? rows : rows + ns;
+}
 __host__ __device__ inline size_t cluster_smem_bytes(int rows, int W, int esz) {
-  return static_cast<size_t>(rows) * W * esz + static_cast<size_t>(W) * 4;
+  return static_cast<size_t>(cluster_slots(rows, esz)) * W * esz;
+}
+// First slot of q_k's slice: ns slots that do not hold row k.
+__host__ __device__ inline int cluster_q_slot(int k, int rows, int esz) {
+  const int ns = cluster_q_slots(esz);
+  if (k >= ns) return 0;
+  return k + 1 + ns <= rows ? k + 1 : rows;
 }
 
 template <typename T>
@@ -77,7 +90,6 @@ __global__ void __launch_bounds__(kCThreads, 1) sv_cluster_kernel(Params p, int 
   const int wr = cluster_warp_range(ne);
   const int run = wr / 32;  // elements per lane run
   T *rows = reinterpret_cast<T *>(smem);
-  float *qs = reinterpret_cast<float *>(smem + static_cast<size_t>(R) * W * sizeof(T));
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kCMaxRows; ++i) mbar_init(smem_addr(&row_bar_s[i]), 1);
@@ -181,7 +193,15 @@ __global__ void __launch_bounds__(kCThreads, 1) sv_cluster_kernel(Params p, int 
   // the bonus row), summed per lane run, per warp range and per slice.
   const bool sample = valid_s && !greedy;
   const bool has_q = sample && dc.xk >= 0 && p.q != nullptr;
+  // q_k's slice goes to slots no longer needed (every row's statistics are
+  // done; row k stays).
+  float *qs = reinterpret_cast<float *>(
+      rows + static_cast<size_t>(cluster_q_slot(sample ? dc.k : 0, R, sizeof(T))) * W);
   if (has_q && threadIdx.x == 0) {
+    // The slots were last read through the generic proxy (the row pass,
+    // ordered before this by the barriers above); the copy writes them
+    // through the async proxy.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     const uint32_t bar = smem_addr(&q_bar_s);
     if (ne > 0) {
       const uint32_t bytes = static_cast<uint32_t>(ne) * 4u;

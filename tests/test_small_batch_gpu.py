@@ -45,6 +45,10 @@ SHAPES = [
     (16, 3, 32000, "bf16", (1.0,), (1, 3), True),
     (32, 2, 50000, "bf16", (0.0, 0.7), None, True),        # the largest batch of the path
     (2, 7, 151936, "bf16", (0.8,), None, True),
+    (8, 8, 128256, "bf16", (0.0, 1.0), None, True),        # q_k's slice in other rows' slots
+    (4, 1, 3000, "fp32", (1.0,), None, True),              # two rows: q needs an extra slot
+    (6, 2, 5000, "bf16", (0.8,), None, True),              # three rows
+    (5, 3, 6000, "bf16", (0.8, 1.0), None, True),          # four rows
 ]
 
 
