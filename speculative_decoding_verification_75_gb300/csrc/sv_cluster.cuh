@@ -11,15 +11,17 @@
 //      its request with 1-D TMA copies (all rows at once) and reduces each
 //      row slice to (maximum, sum) -- or (maximum, lowest argmax) for a
 //      greedy row -- with the same chunk statistics as the persistent kernel;
-//   2. after a cluster barrier every CTA reads the slices' statistics of all
-//      CTAs from their shared memory, combines them in rank order and runs
-//      the same accept step (so every CTA knows the first rejection k; only
-//      rank 0 writes outputs);
+//   2. each CTA stores its slices' statistics into the shared memory of
+//      every CTA of the cluster (distributed shared memory); after a
+//      cluster barrier every CTA combines them in rank order from its own
+//      shared memory and runs the same accept step (so every CTA knows the
+//      first rejection k; only rank 0 writes outputs);
 //   3. a sampled request's CTAs form r = (p_k - q_k)_+ (or p_k) on the row-k
 //      slice they still hold, loading only their slice of q_k, and sum it per
 //      lane run, per warp and per slice;
-//   4. after a second barrier every CTA reads the slice sums, the slice that
-//      holds u * S walks its warps, then its lanes' runs, to the token.
+//   4. the slice sums are pushed the same way; after a second barrier the
+//      slice that holds u * S walks its warps, then its lanes' runs, to the
+//      token.  No CTA touches a peer's shared memory after that barrier.
 //
 // The logits are read once (row k is not re-read) and q only at the
 // rejected row.  Decisions use the same arithmetic as the persistent path;
@@ -71,10 +73,10 @@ __global__ void __launch_bounds__(kCThreads, 1) sv_cluster_kernel(Params p, int 
   __shared__ uint64_t row_bar_s[kCMaxRows];
   __shared__ uint64_t q_bar_s;
   __shared__ Part wstat_s[kCMaxRows][kCWarps];  // per row, per warp range
-  __shared__ float2 part_s[kCMaxRows];          // per row: this slice's statistics
+  __shared__ float2 part_s[kCMaxCluster][kCMaxRows];  // per rank, per row: slice statistics
   __shared__ float2 wsum_s[kCWarps];            // residual / p sums per warp range
   __shared__ float2 lsum_s[kCWarps][32];        // ... and per lane run
-  __shared__ float2 rsum_s;                     // ... and of the slice
+  __shared__ float2 rsum_s[kCMaxCluster];       // ... and of every rank's slice
   __shared__ DraftIn din_s[kCMaxRows];
   __shared__ Ctl ctl_s;
   __shared__ Decision dec_s;
@@ -98,6 +100,9 @@ __global__ void __launch_bounds__(kCThreads, 1) sv_cluster_kernel(Params p, int 
     fence_mbar_init();
   }
   __syncthreads();
+  // Every CTA of the cluster must have started before any writes into a
+  // peer's shared memory: arrive now, wait before the first such write.
+  cluster_arrive_relaxed();
   pdl_wait();
   pdl_launch_dependents();
 
@@ -139,6 +144,7 @@ __global__ void __launch_bounds__(kCThreads, 1) sv_cluster_kernel(Params p, int 
     if (lane == 0) wstat_s[i][warp] = Part{st.m, st.v};
   }
   __syncthreads();
+  cluster_wait();
   if (warp == 0 && lane < nr) {
     Part q[kMergeBatch];
 #pragma unroll
@@ -147,9 +153,12 @@ __global__ void __launch_bounds__(kCThreads, 1) sv_cluster_kernel(Params p, int 
     float m = -INFINITY, s = 0.f;
     int am = -1;
     fold_batch(q, kCWarps, cs, m, s, am);
-    part_s[lane] = make_float2(m, greedy ? __int_as_float(am) : s);
+    // pushed into every CTA of the cluster (this one included): after the
+    // barrier each reads them from its own shared memory
+    const float2 v = make_float2(m, greedy ? __int_as_float(am) : s);
+    for (uint32_t r2 = 0; r2 < CS; ++r2) st_peer_f2(&part_s[rank][lane], r2, v);
   }
-  cluster_sync();  // every slice's statistics are visible to the cluster
+  cluster_sync();  // every slice's statistics are in every CTA
 
   // 2. Every CTA: the rows' statistics over all slices, in rank order, and
   // the accept step; rank 0 writes the outputs.
@@ -168,7 +177,7 @@ __global__ void __launch_bounds__(kCThreads, 1) sv_cluster_kernel(Params p, int 
         Part q[kMergeBatch];
 #pragma unroll
         for (int tj = 0; tj < kMergeBatch; ++tj) {
-          const float2 v = tj < static_cast<int>(CS) ? ld_peer_f2(&part_s[lane], tj)
+          const float2 v = tj < static_cast<int>(CS) ? part_s[tj][lane]
                                                      : make_float2(-INFINITY, 0.f);
           q[tj] = Part{v.x, v.y};
         }
@@ -276,10 +285,12 @@ __global__ void __launch_bounds__(kCThreads, 1) sv_cluster_kernel(Params p, int 
         sr = __fadd_rn(sr, wsum_s[w].x);
         sp = __fadd_rn(sp, wsum_s[w].y);
       }
-      rsum_s = make_float2(sr, sp);
+      for (uint32_t r2 = 0; r2 < CS; ++r2) st_peer_f2(&rsum_s[rank], r2, make_float2(sr, sp));
     }
   }
-  cluster_sync();  // every slice's sums are visible to the cluster
+  // Every slice's sums are in every CTA.  No CTA touches a peer's shared
+  // memory after this barrier, so each may leave when it is done.
+  cluster_sync();
 
   // 4. The draw: the slice, then the warp range, then the lane run holding
   // u * S (S the residual mass, or p's when the residual is empty).
@@ -287,8 +298,7 @@ __global__ void __launch_bounds__(kCThreads, 1) sv_cluster_kernel(Params p, int 
   __shared__ float draw_base_s, draw_target_s;
   __shared__ int draw_use_p_s;
   if (sample && warp == 0) {
-    const float2 v = lane < static_cast<int>(CS) ? ld_peer_f2(&rsum_s, lane)
-                                                 : make_float2(0.f, 0.f);
+    const float2 v = lane < static_cast<int>(CS) ? rsum_s[lane] : make_float2(0.f, 0.f);
     const float tr = __shfl_sync(kFull, warp_inclusive_scan(v.x, lane), 31);
     const float tp = __shfl_sync(kFull, warp_inclusive_scan(v.y, lane), 31);
     const bool use_p = !(tr > 0.f);  // empty residual: draw from p itself
@@ -349,7 +359,6 @@ __global__ void __launch_bounds__(kCThreads, 1) sv_cluster_kernel(Params p, int 
     }
     if (lane == 0) p.out_tokens[static_cast<size_t>(b) * R + dc.k] = tok;
   }
-  cluster_sync();  // no CTA leaves while a peer may read its shared memory
 
   if (threadIdx.x == 0) {
     // The call's error word, and the epoch: the grid's last CTA advances it.
