@@ -71,16 +71,12 @@ namespace sv {
 #ifndef SV_PREFETCH_NS
 #define SV_PREFETCH_NS 3000
 #endif
-#ifndef SV_ROWS_FIRST
-#define SV_ROWS_FIRST 0
-#endif
 constexpr int kPairs = SV_PAIRS;             // consumer pairs
 constexpr int kStages = SV_STAGES;
 constexpr int kRowBlock = SV_ROW_BLOCK;      // row-statistics items per claim
 constexpr int kResBlock = SV_RES_BLOCK;      // residual items per claim
 constexpr int kClaimSlots = SV_CLAIM_SLOTS;  // claimed blocks queued ahead
 constexpr unsigned kPollNs = SV_POLL_NS;      // pause between polls of a global flag
-constexpr bool kRowsFirst = SV_ROWS_FIRST != 0;  // residual work only once rows are gone
 // A job warp whose merge is not due this long after it took the ticket
 // gathers the merge's draft inputs (ids, uniforms, l(x), q(x)) while it
 // waits, so the merge itself needs one wave of loads.  Early merges never
@@ -497,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
     bool rows_left = true, more = true;
     while (ok && more) {
       if (rows_left) {
-        const uint2 bc = kRowsFirst ? make_uint2(0u, 0u) : ld_relaxed2(&c.ctr->b_next);
+        const uint2 bc = ld_relaxed2(&c.ctr->b_next);  // {b_next, b_reserved}
         const uint32_t sl = bc.x / C2;
         if (sl < bc.y) {
           Desc d;
