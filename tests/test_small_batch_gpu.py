@@ -95,3 +95,24 @@ def test_invalid_inputs(path):
     assert ora["bad"].tolist() == [0, 1, 2, 4, 8, 16, 32, 2]
     rc, word = api.last_error(api.get_workspace(B, g, V, DEV))
     assert rc == api.SV_ERR_BAD_INPUT_DATA and word == 1 | 2 | 4 | 8 | 16 | 32
+
+
+def test_greedy_ties_across_slices(path):
+    """A greedy row whose maximum appears in several places -- inside one
+    slice / chunk and across slices, chunks and clusters' ranks -- takes the
+    lowest index, as the oracle does."""
+    B, g, V = 4, 3, 40000
+    w = Workload("ties", B, g, V, "bf16", 1.0, (0.5, 0.5), (0.0,), seed=43)
+    case = make_case(w, device=DEV)
+    lg = case["logits"]
+    spots = [[39990, 17, 25000], [5, 6, 30001], [20000, 39999, 2500], [12345, 12346, 12347]]
+    for b in range(B):
+        for i in range(g + 1):
+            for j, pos in enumerate(spots[(b + i) % B]):
+                lg[b, i, pos] = 50.0  # far above every other logit
+    gpu = run_gpu(case)
+    ora = run_oracle(case)
+    compare(case, gpu, ora)
+    for b in range(B):
+        k = int(gpu["num_accepted"][b])
+        assert gpu["tokens"][b][k] == min(spots[(b + k) % B])
