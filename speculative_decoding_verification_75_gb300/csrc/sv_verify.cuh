@@ -73,7 +73,13 @@ namespace sv {
 #endif
 constexpr int kPairs = SV_PAIRS;             // consumer pairs
 constexpr int kStages = SV_STAGES;
-constexpr int kRowBlock = SV_ROW_BLOCK;      // row-statistics items per claim
+constexpr int kRowBlock = SV_ROW_BLOCK;      // row-statistics items per claim (base)
+// Large batches claim bigger row blocks -- about kRowBlocksPerCta of them per
+// CTA, up to kRowBlockMax items -- which halves the claims of c5 (106.2 vs
+// 108.0 us); at c3 and c4 the base size stays (bigger blocks there delay the
+// last requests' merges).
+constexpr int kRowBlockMax = 16;
+constexpr int kRowBlocksPerCta = 6;
 constexpr int kResBlock = SV_RES_BLOCK;      // residual items per claim
 // Claimed blocks queued ahead of the producer.  One: a deeper queue holds
 // rows (and residual work) claimed early behind a CTA's staged items, so the
@@ -454,12 +460,16 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
     const uint32_t n_rows = uniform ? static_cast<uint32_t>(p.B) * R
                                     : static_cast<uint32_t>(row_start(p.B));
     const uint32_t n_row_items = n_rows * static_cast<uint32_t>(p.C1);
-    const uint32_t rb =
+    const uint32_t rb_base =
         min(static_cast<uint32_t>(kRowBlock), max(1u, n_row_items / (2u * gridDim.x)));
+    const uint32_t rb =
+        min(static_cast<uint32_t>(kRowBlockMax),
+            max(rb_base, n_row_items / (static_cast<uint32_t>(kRowBlocksPerCta) * gridDim.x)));
     const uint32_t a_dyn = rb * gridDim.x;  // first item handed out by the counter
     const uint32_t C2 = static_cast<uint32_t>(p.C2);
-    // Claim sizes: up to kRowBlock / kResBlock items, fewer when the batch
-    // is small, so that its items spread over the grid.
+    // Claim sizes: kRowBlock / kResBlock items, fewer when the batch is small
+    // (so that its items spread over the grid), and for rows more when it is
+    // large.
     const uint32_t spread = 2u * gridDim.x;
     const uint32_t rt =
         min(static_cast<uint32_t>(kResBlock), max(1u, static_cast<uint32_t>(p.B) * C2 / spread));
