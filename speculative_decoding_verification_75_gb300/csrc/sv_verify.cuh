@@ -1,7 +1,9 @@
 // sv_verify.cuh -- the persistent verification kernel.
 //
-// One CTA per SM runs the whole verification step of a batch (after the
-// small set-up kernel 0), on two kinds of work item:
+// One CTA per SM runs the whole verification step of a batch in one launch
+// (the small set-up kernel 0 runs first only for batches beyond the shared
+// tables' 256 requests or when the acceptance histogram is asked for), on
+// two kinds of work item:
 //
 //   row-statistics items  every (active row, vocabulary chunk) of the target
 //                         logits, handed out from a global counter in blocks,
@@ -14,10 +16,12 @@
 //                         requests' merges publish their rows.
 //
 // Because row blocks go out request after request, requests complete while
-// the stream runs, and the row a request draws from was read moments before:
-// its re-read is mostly served by L2.  No CTA ever waits for a specific other
-// CTA: all work is claimed dynamically, so progress does not depend on which
-// CTAs are resident.
+// the stream runs, and the residual work of each request overlaps the rows
+// of later ones.  Every byte streams with an evict-first L2 policy, so the
+// re-read of a drawn row comes from DRAM (keeping rows, or only every
+// request's row 0, resident in L2 measured no faster overall).  No CTA ever
+// waits for a specific other CTA: all work is claimed dynamically, so
+// progress does not depend on which CTAs are resident.
 //
 // Roles inside a CTA:
 //   claimer lane    claims blocks of work (all the global round trips of
