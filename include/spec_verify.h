@@ -276,10 +276,9 @@ SV_API const char *sv_status_string(sv_status status);
  *     1 MiB).
  *   - The first call on a device looks up the scratch array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it for the
- *     rest of the process; make that first call before capturing any stream
- *     on the device.  The cached address does not survive a reset of the
- *     device's primary context (cudaDeviceReset): calling this entry point
- *     after such a reset is not supported.
+ *     rest of the process.  The cached address does not survive a reset of
+ *     the device's primary context (cudaDeviceReset): calling this entry
+ *     point after such a reset is not supported.
  *   - Every call on a device shares the one array, which each call leaves
  *     ready for the next; calls whose work may overlap on the GPU (other
  *     streams, other host threads) race on it and must be serialised by the
