@@ -374,8 +374,13 @@ def run_ours(args, rank, local_rank, world):
     return line
 
 
+# The five workloads, c4's gamma 3..8 (B = 64, V = 128256), and c3's shape
+# (gamma = 5, peaky rows) along the other two axes: V = 32000 and 128256 at
+# B = 128, B = 32 and 256 at V = 151936.
 SWEEP = [("c1", {}), ("c2", {}), ("c3", {}), ("c4", {}), ("c5", {})] + \
-    [(f"c4_gamma{g}", {"gamma": g}) for g in range(3, 9)]
+    [(f"c4_gamma{g}", {"gamma": g}) for g in range(3, 9)] + \
+    [("c3_V32000", {"V": 32000}), ("c3_V128256", {"V": 128256}),
+     ("c3_B32", {"B": 32}), ("c3_B256", {"B": 256})]
 
 
 def sweep(api, W, dev, args, peak):
@@ -390,7 +395,8 @@ def sweep(api, W, dev, args, peak):
         w = W.workload(key.split("_")[0], **over)
         r = time_workload(api, W, w, dev, args.sweep_steps, 3, flush)
         gbs = r["bytes_per_step"] / (r["us_per_step"] * 1e-6) / 1e9
-        out[key] = {"workload": w.name if not over else f"{w.name} (gamma={w.gamma})",
+        label = ", ".join(f"{k}={v}" for k, v in over.items())
+        out[key] = {"workload": w.name if not over else f"{w.name} ({label})",
                     "B": w.B, "gamma": w.gamma, "V": w.V, "dtype": w.dtype,
                     "us_per_step": r["us_per_step"], "rows_per_s": r["rows_per_s"],
                     "gbs": gbs, "frac": gbs / peak, "alpha_hat": r["alpha_hat"],
