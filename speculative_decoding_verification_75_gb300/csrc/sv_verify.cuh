@@ -79,16 +79,17 @@ constexpr int kPairs = SV_PAIRS;             // consumer pairs
 constexpr int kStages = SV_STAGES;
 constexpr int kRowBlock = SV_ROW_BLOCK;      // row-statistics items per claim (base)
 // Large batches claim bigger row blocks -- about kRowBlocksPerCta of them per
-// CTA, up to kRowBlockMax items -- which halves the claims of c5 (106.2 vs
-// 108.0 us); at c3 and c4 the base size stays (bigger blocks there delay the
-// last requests' merges).
+// CTA, up to kRowBlockMax items -- which halves the row claims of 256 ragged
+// requests at V = 151936 (106.2 vs 108.0 us); 128 requests of 6 rows and 64
+// of 9 keep the base size (bigger blocks there delay the last merges).
 constexpr int kRowBlockMax = 16;
 constexpr int kRowBlocksPerCta = 6;
 constexpr int kResBlock = SV_RES_BLOCK;      // residual items per claim
 // Claimed blocks queued ahead of the producer.  One: a deeper queue holds
 // rows (and residual work) claimed early behind a CTA's staged items, so the
 // last requests' merges, and the residual work that follows them, start later
-// (c4 50.2 us with two, 46.3 us with one; c3 and c5 unchanged or better).
+// (64 requests of 9 bf16 rows of 128256 logits: 50.2 us with two, 46.3 us
+// with one; larger batches unchanged or faster).
 constexpr int kClaimSlots = SV_CLAIM_SLOTS;
 constexpr unsigned kPollNs = SV_POLL_NS;      // pause between polls of a global flag
 // A job warp whose merge is not due this long after it took the ticket
@@ -574,8 +575,9 @@ __global__ void __launch_bounds__(kThreads, 1) sv_verify_kernel(Params p) {
     // -------------------------------------------------- producer lane ----
 // Every logit and q value is streamed with an evict-first L2 policy: the
     // row statistics read each logit once, and keeping rows in L2 for the
-    // residual re-read measured slower (c3 65.2 vs 64.1 us with evict-normal
-    // rows, the same with evict-last).
+    // residual re-read measured slower (65.2 vs 64.1 us for 128 requests of 6
+    // bf16 rows of 151936 logits with evict-normal rows, the same with
+    // evict-last).
     const uint64_t pol_l = policy_evict_first(), pol_q = pol_l, pol_r = pol_l;
     uint32_t n = 0, m = 0, pushed = 0;  // items issued / observed released; runs handed over
     bool ok = true;
