@@ -327,35 +327,73 @@ __global__ void __launch_bounds__(kCThreads, 1) sv_cluster_kernel(Params p, int 
   }
   __syncthreads();
   if (sample && warp == draw_warp_s) {
-    // Each lane walks its run from its exclusive prefix; the first lane to
-    // pass the target holds the token.
     const bool use_p = draw_use_p_s != 0;
     const float base = draw_base_s, target = draw_target_s;
     const float lw = use_p ? lsum_s[warp][lane].y : lsum_s[warp][lane].x;
     const float incl = base + warp_inclusive_scan(lw, lane);
     const float prev = __shfl_up_sync(kFull, incl, 1);
-    float c = (lane == 0) ? base : prev;
-    const int l0 = warp * wr + lane * run;
-    int hit = -1, lastpos = -1;
-    for (int j0 = l0; j0 < min(l0 + run, ne) && hit < 0; j0 += 8) {
+    const float excl = (lane == 0) ? base : prev;
+    int tok = -1;
+    // The first lane whose inclusive prefix passes the target holds the
+    // token.  For runs of more than two vectors the whole warp walks that
+    // lane's run, a vector of 8 per lane, each vector from its exclusive
+    // prefix within the run: one vector's weights per lane instead of a
+    // run's (8 requests at V = 151936: 14.1 vs 14.9 us a step; for shorter
+    // runs the extra scan costs more than it saves).
+    const unsigned pass = __ballot_sync(kFull, incl > target);
+    if (pass && run > 16 && run <= 8 * 32) {
+      const int L = __ffs(pass) - 1;
+      const float start = __shfl_sync(kFull, excl, L);
+      const int j0 = warp * wr + L * run + 8 * lane;
+      const bool mine = 8 * lane < run && j0 < ne;
       float pw[8], rw[8];
-      weights8(j0, pw, rw);
+      float vs = 0.f;
+      if (mine) {
+        weights8(j0, pw, rw);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float w = use_p ? pw[u] : rw[u];
-        c = __fadd_rn(c, w);
-        if (hit < 0 && c > target) hit = j0 + u;
-        if (w > 0.f) lastpos = j0 + u;
+        for (int u = 0; u < 8; ++u) vs = __fadd_rn(vs, use_p ? pw[u] : rw[u]);
       }
+      const float vincl = warp_inclusive_scan(vs, lane);
+      const float vprev = __shfl_up_sync(kFull, vincl, 1);
+      float c = (lane == 0) ? start : __fadd_rn(start, vprev);
+      int hit = -1;
+      if (mine) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          c = __fadd_rn(c, use_p ? pw[u] : rw[u]);
+          if (hit < 0 && c > target) hit = j0 + u;
+        }
+      }
+      const unsigned hb = __ballot_sync(kFull, hit >= 0);
+      if (hb) tok = e0 + __shfl_sync(kFull, hit, __ffs(hb) - 1);
     }
-    int tok = e0;
-    const unsigned hb = __ballot_sync(kFull, hit >= 0);
-    if (hb) {
-      tok = e0 + __shfl_sync(kFull, hit, __ffs(hb) - 1);
-    } else {
-      // Rounding left u*S at or past the total: the last positive weight.
-      const unsigned pb = __ballot_sync(kFull, lastpos >= 0);
-      if (pb) tok = e0 + __shfl_sync(kFull, lastpos, 31 - __clz(pb));
+    if (tok < 0) {
+      // Rounding kept the walk of that run below the target, or u*S lies at
+      // or past the total: each lane walks its own run from its exclusive
+      // prefix; the first lane to pass the target holds the token, else the
+      // last positive weight.
+      float c = excl;
+      const int l0 = warp * wr + lane * run;
+      int hit = -1, lastpos = -1;
+      for (int j0 = l0; j0 < min(l0 + run, ne) && hit < 0; j0 += 8) {
+        float pw[8], rw[8];
+        weights8(j0, pw, rw);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float w = use_p ? pw[u] : rw[u];
+          c = __fadd_rn(c, w);
+          if (hit < 0 && c > target) hit = j0 + u;
+          if (w > 0.f) lastpos = j0 + u;
+        }
+      }
+      tok = e0;
+      const unsigned hb = __ballot_sync(kFull, hit >= 0);
+      if (hb) {
+        tok = e0 + __shfl_sync(kFull, hit, __ffs(hb) - 1);
+      } else {
+        const unsigned pb = __ballot_sync(kFull, lastpos >= 0);
+        if (pb) tok = e0 + __shfl_sync(kFull, lastpos, 31 - __clz(pb));
+      }
     }
     if (lane == 0) p.out_tokens[static_cast<size_t>(b) * R + dc.k] = tok;
   }
