@@ -334,13 +334,15 @@ __global__ void __launch_bounds__(kCThreads, 1) sv_cluster_kernel(Params p, int 
     const float prev = __shfl_up_sync(kFull, incl, 1);
     const float excl = (lane == 0) ? base : prev;
     int tok = -1;
-    // The first lane whose inclusive prefix passes the target holds the
-    // token.  For runs of more than two vectors the whole warp walks that
+    // The first lane with weight whose inclusive prefix passes the target
+    // holds the token (as at every level of the draw, an index without
+    // weight is never chosen, even where rounding puts its prefix past the
+    // target).  For runs of more than two vectors the whole warp walks that
     // lane's run, a vector of 8 per lane, each vector from its exclusive
     // prefix within the run: one vector's weights per lane instead of a
     // run's (8 requests at V = 151936: 14.1 vs 14.9 us a step; for shorter
     // runs the extra scan costs more than it saves).
-    const unsigned pass = __ballot_sync(kFull, incl > target);
+    const unsigned pass = __ballot_sync(kFull, lw > 0.f && incl > target);
     if (pass && run > 16 && run <= 8 * 32) {
       const int L = __ffs(pass) - 1;
       const float start = __shfl_sync(kFull, excl, L);
@@ -360,8 +362,9 @@ __global__ void __launch_bounds__(kCThreads, 1) sv_cluster_kernel(Params p, int 
       if (mine) {
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          c = __fadd_rn(c, use_p ? pw[u] : rw[u]);
-          if (hit < 0 && c > target) hit = j0 + u;
+          const float wu = use_p ? pw[u] : rw[u];
+          c = __fadd_rn(c, wu);
+          if (hit < 0 && wu > 0.f && c > target) hit = j0 + u;
         }
       }
       const unsigned hb = __ballot_sync(kFull, hit >= 0);
@@ -382,7 +385,7 @@ __global__ void __launch_bounds__(kCThreads, 1) sv_cluster_kernel(Params p, int 
         for (int u = 0; u < 8; ++u) {
           const float w = use_p ? pw[u] : rw[u];
           c = __fadd_rn(c, w);
-          if (hit < 0 && c > target) hit = j0 + u;
+          if (hit < 0 && w > 0.f && c > target) hit = j0 + u;
           if (w > 0.f) lastpos = j0 + u;
         }
       }

@@ -40,8 +40,9 @@ __device__ __forceinline__ float2 target_p2(float2 x, float2 nego, float2 cs2, f
 
 // One level of the inverse-CDF walk over n <= 64 weights held two per lane
 // (w0 for index lane, w1 for lane + 32), starting at `carry`: the first index
-// whose inclusive prefix exceeds target, else the last index with positive
-// weight (then *fell_back is set).  Also returns the exclusive prefix.
+// with positive weight whose inclusive prefix exceeds target, else the last
+// index with positive weight (then *fell_back is set).  Also returns the
+// exclusive prefix.
 __device__ __forceinline__ int cdf_level64(int n, float w0, float w1, float carry,
                                            float target, int lane, float *excl_out,
                                            bool *fell_back) {
@@ -54,7 +55,7 @@ __device__ __forceinline__ int cdf_level64(int n, float w0, float w1, float carr
     const float incl = carry + warp_inclusive_scan(w, lane);
     const float prev = __shfl_up_sync(kFull, incl, 1);
     const float excl = (lane == 0) ? carry : prev;
-    const unsigned hit = __ballot_sync(kFull, i < n && incl > target);
+    const unsigned hit = __ballot_sync(kFull, i < n && w > 0.f && incl > target);
     if (hit) {
       const int src = __ffs(hit) - 1;
       *excl_out = __shfl_sync(kFull, excl, src);
@@ -85,7 +86,7 @@ __device__ __forceinline__ int cdf_level(int n, float carry, float target, int l
     const float incl = carry + warp_inclusive_scan(w, lane);
     const float prev = __shfl_up_sync(kFull, incl, 1);
     const float excl = (lane == 0) ? carry : prev;
-    const unsigned hit = __ballot_sync(kFull, i < n && incl > target);
+    const unsigned hit = __ballot_sync(kFull, i < n && w > 0.f && incl > target);
     if (hit) {
       const int src = __ffs(hit) - 1;
       *excl_out = __shfl_sync(kFull, excl, src);
@@ -177,7 +178,7 @@ __device__ __forceinline__ int search_segment(const Params &p, const Desc &d, in
 #pragma unroll
   for (int t = 0; t < 32; ++t) {
     c += w[t];
-    if (hit < 0 && c > target) hit = t;
+    if (hit < 0 && w[t] > 0.f && c > target) hit = t;
     if (w[t] > 0.f) lastpos = t;
   }
   const unsigned hb = __ballot_sync(kFull, hit >= 0);
@@ -193,9 +194,12 @@ __device__ __forceinline__ int search_segment(const Params &p, const Desc &d, in
 }
 
 // Inverse-CDF walk over n <= 256 weights held eight per lane, lane l owning
-// indices 8l..8l+7 in order: the first index whose inclusive prefix exceeds
-// target, else the last index with positive weight (then *fell_back is set).
-// Also returns the exclusive prefix at that index.
+// indices 8l..8l+7 in order: the first index with positive weight whose
+// inclusive prefix exceeds target, else the last index with positive weight
+// (then *fell_back is set).  Also returns the exclusive prefix at that index.
+// Every level of the draw skips zero weights this way: with u * S within
+// rounding of the total, a scanned prefix can pass the target at an index
+// that holds nothing (a padded lane past the end of the row included).
 __device__ __forceinline__ int cdf_block8(int n, const float (&w)[8], float target, int lane,
                                           float *excl_out, bool *fell_back) {
   float tot = 0.f;
@@ -210,7 +214,7 @@ __device__ __forceinline__ int cdf_block8(int n, const float (&w)[8], float targ
   for (int j = 0; j < 8; ++j) {
     const bool in = 8 * lane + j < n;
     const float wj = in ? w[j] : 0.f;
-    if (in && hit < 0 && c + wj > target) {
+    if (in && hit < 0 && wj > 0.f && c + wj > target) {
       hit = j;
       hit_excl = c;
     }

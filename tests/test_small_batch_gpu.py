@@ -8,6 +8,7 @@ slices that are empty (V smaller than the cluster), ragged vocabulary
 tails, gamma up to 15, greedy / sampled / mixed temperatures, deterministic
 drafts, an all-accepting draft (bonus draws) and invalid inputs.
 """
+import numpy as np
 import pytest
 import torch
 
@@ -116,3 +117,23 @@ def test_greedy_ties_across_slices(path):
     for b in range(B):
         k = int(gpu["num_accepted"][b])
         assert gpu["tokens"][b][k] == min(spots[(b + k) % B])
+
+
+@pytest.mark.parametrize("V", [40000, 151936])
+def test_sample_uniform_extremes(path, V):
+    """u_sample at 0 (the first token with positive mass) and at the largest
+    binary32 value below 1 (u * S at or within rounding of the total: the
+    walk may end past every weight and take the last positive one), on
+    residual draws and on bonus draws.  At V = 151936 each lane's run of a
+    cluster slice is several vectors (the draw walks the one run that holds
+    the target); at V = 40000 a run is one vector."""
+    B, g = 8, 3
+    w = Workload(f"u extremes V={V}", B, g, V, "bf16", 2.0, (0.5, 1.5), (0.8, 1.0), seed=44)
+    case = make_case(w, device=DEV)
+    top = float(np.nextafter(np.float32(1.0), np.float32(0.0)))
+    case["u_sample"][:] = torch.tensor([0.0, top] * (B // 2), device=DEV)
+    case["u_accept"][:2] = 0.0  # every draft accepted: bonus draws
+    gpu = run_gpu(case)
+    rep = compare(case, gpu, run_oracle(case))
+    assert rep["bad"] == 0 and rep["borderline"] <= 1
+    assert (torch.as_tensor(gpu["num_accepted"][:2]) == g).all()
