@@ -13,7 +13,11 @@
  *     rejection, from p_{g_b} (the bonus row, §5.3) when all are kept.
  *   Draws are inverse-CDF draws on the caller's uniform u_s[b]: the token is
  *   the smallest j whose inclusive prefix sum of the (unnormalised) weights
- *   exceeds u_s[b] times their total.  T_b = 0 is greedy decoding (P3 §8,
+ *   exceeds u_s[b] times their total, so a token without weight is never
+ *   drawn; where binary32 rounding leaves u_s[b] times the total at or past
+ *   the summed weights, the last token with positive weight.  An empty
+ *   residual (every (p - q)_+ zero) draws from p_k instead.  T_b = 0 is
+ *   greedy decoding (P3 §8,
  *   pitfall 2): p is one-hot at the lowest-index maximum logit.
  *
  * Conventions for every entry point:
