@@ -86,6 +86,8 @@ class Oracle:
         lib.orc_draw_cdf.restype = ctypes.c_int
         lib.orc_draw_cdf.argtypes = [_P, ctypes.c_int, _P, _P, _P, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
+        lib.orc_draw_weights.restype = ctypes.c_int
+        lib.orc_draw_weights.argtypes = lib.orc_draw_cdf.argtypes
         lib.orc_inverse_cdf.restype = ctypes.c_int
         lib.orc_inverse_cdf.argtypes = [_P, ctypes.c_int, ctypes.c_double, _P]
         self.lib = lib
@@ -145,6 +147,17 @@ class Oracle:
         """Inclusive prefix sums (fp64, [V]) of the weights of the draw at
         position k of request b (g its draft length), as the oracle walks
         them; None for a greedy request."""
+        return self._draw(self.lib.orc_draw_cdf, logits, draft_ids, draft_probs, temperature,
+                          b, k, g)
+
+    def draw_weights(self, logits, draft_ids, draft_probs, temperature, b: int, k: int,
+                     g: int):
+        """The weights themselves (fp64, [V]) of that draw; None for a greedy
+        request."""
+        return self._draw(self.lib.orc_draw_weights, logits, draft_ids, draft_probs,
+                          temperature, b, k, g)
+
+    def _draw(self, fn, logits, draft_ids, draft_probs, temperature, b, k, g):
         arr, is_bf16 = logits_to_numpy(logits)
         arr = np.ascontiguousarray(arr)
         B, rows, V = arr.shape
@@ -152,10 +165,10 @@ class Oracle:
         ids = _c(_np(draft_ids).reshape(B, gmax), np.int32)
         q = None if draft_probs is None else _c(_np(draft_probs).reshape(B, gmax, V), np.float32)
         T = _c(_np(temperature).reshape(B), np.float32)
-        cdf = np.empty(V, np.float64)
-        rc = self.lib.orc_draw_cdf(_ptr(arr), int(bool(is_bf16)), _ptr(ids), _ptr(q), _ptr(T),
-                                   int(b), int(k), int(g), gmax, V, _ptr(cdf))
-        return None if rc != 0 else cdf
+        out = np.empty(V, np.float64)
+        rc = fn(_ptr(arr), int(bool(is_bf16)), _ptr(ids), _ptr(q), _ptr(T),
+                int(b), int(k), int(g), gmax, V, _ptr(out))
+        return None if rc != 0 else out
 
     def row_stats(self, row, temperature: float):
         """(max, normaliser, argmax) of the softmax of row / T for one row."""

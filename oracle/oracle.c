@@ -467,14 +467,14 @@ int orc_verify_mt(const void *logits, int is_bf16, const int32_t *draft_ids,
     return rc;
 }
 
-/* Test support: the inclusive prefix sums C_0 .. C_{V-1} of the weights the
- * draw at position k of request b walks (draw_weights, with the request's
- * row statistics recomputed), so that a drawn token j can be checked against
- * its interval [C_{j-1}, C_j) when u * C_{V-1} falls near an edge.  Returns 0,
- * or -1 for T <= 0 (no draw) or an allocation failure. */
-int orc_draw_cdf(const void *logits, int is_bf16, const int32_t *draft_ids,
-                 const float *draft_probs, const float *temperature, int b, int k, int g,
-                 int gmax, int V, double *cdf)
+/* Test support: the weights w_0 .. w_{V-1} that the draw at position k of
+ * request b walks (draw_weights, with the request's row statistics
+ * recomputed), so that a drawn token's own mass can be checked even where it
+ * lies below the resolution of the prefix sums.  Returns 0, or -1 for T <= 0
+ * (no draw). */
+int orc_draw_weights(const void *logits, int is_bf16, const int32_t *draft_ids,
+                     const float *draft_probs, const float *temperature, int b, int k,
+                     int g, int gmax, int V, double *w)
 {
     const double T = (double)temperature[b];
     if (!(T > 0.0)) return -1;
@@ -483,7 +483,21 @@ int orc_draw_cdf(const void *logits, int is_bf16, const int32_t *draft_ids,
     int argmax, fallback;
     orc_row_stats(logits, is_bf16, off, V, T, &mx, &s, &argmax);
     draw_weights(logits, is_bf16, draft_ids, draft_probs, b, k, g, gmax, V, off, mx, s,
-                 argmax, T, cdf, &fallback);
+                 argmax, T, w, &fallback);
+    return 0;
+}
+
+/* Test support: the inclusive prefix sums C_0 .. C_{V-1} of those weights,
+ * so that a drawn token j can be checked against its interval
+ * [C_{j-1}, C_j) when u * C_{V-1} falls near an edge.  Returns 0, or -1 for
+ * T <= 0 (no draw). */
+int orc_draw_cdf(const void *logits, int is_bf16, const int32_t *draft_ids,
+                 const float *draft_probs, const float *temperature, int b, int k, int g,
+                 int gmax, int V, double *cdf)
+{
+    if (orc_draw_weights(logits, is_bf16, draft_ids, draft_probs, temperature, b, k, g, gmax,
+                         V, cdf) != 0)
+        return -1;
     double c = 0.0;
     for (int j = 0; j < V; ++j) {
         c += cdf[j];
