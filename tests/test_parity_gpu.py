@@ -182,6 +182,29 @@ def test_invalid_inputs_are_isolated():
     assert word == 1 | 2 | 4 | 8 | 16 | 32
 
 
+@pytest.mark.parametrize("V,dt", [(300000, "bf16"), (300001, "fp32")])
+@pytest.mark.parametrize("small_path", [True, False], ids=["cluster", "persistent"])
+def test_very_large_vocabulary(V, dt, small_path):
+    """Rows longer than one batch of chunk statistics (more than 16 chunks
+    per row: the merge folds two batches) and than 256 segments of 1024 (the
+    search walks chunk sums, then the chunk's segment sums, then the
+    segment), aligned (TMA) and odd (plain loads), with sample uniforms at 0
+    and just below 1 as well as random ones."""
+    B, g = 4, 3
+    w = Workload(f"large V={V} {dt}", B, g, V, dt, 2.0, (0.5, 1.5), (0.8, 1.0), seed=45)
+    case = make_case(w, device=DEV)
+    top = float(np.nextafter(np.float32(1.0), np.float32(0.0)))
+    case["u_sample"][0] = 0.0
+    case["u_sample"][1] = top
+    prev = api.set_small_batch_path(small_path)
+    try:
+        gpu = run_gpu(case)
+    finally:
+        api.set_small_batch_path(prev)
+    rep = compare(case, gpu, run_oracle(case))
+    assert rep["bad"] == 0 and rep["borderline"] <= 1
+
+
 @pytest.mark.parametrize("V", [4096, 40000])
 @pytest.mark.parametrize("small_path", [True, False], ids=["cluster", "persistent"])
 def test_tiny_temperature_is_invalid_data(V, small_path):
